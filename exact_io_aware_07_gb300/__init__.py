@@ -1,0 +1,145 @@
+"""FlashAttention forward on one GB300: Python binding of the C-ABI library ``libfa_gb300.so``.
+
+The binding only marshals arguments: it checks tensor dtypes, shapes and
+devices, then passes raw device pointers and the current CUDA stream to the
+C entry points declared in ``include/fa.h``.  Every step of the attention
+computation runs in the library's sm_103a kernel; there is no other path.  If
+the library has not been built, importing works but the first call raises.
+
+Entry points (same names as the C ABI):
+    fa_fwd(q, k, v, o, lse, causal, scale, stream=None)
+    fa_status_string(code), fa_device_status(stream=None)
+    fa_fwd_launch_shape(B, H, T, d, causal, num_sms), fa_version()
+and the convenience wrapper ``attention(q, k, v, causal, scale=None)`` that
+allocates O and LSE with PyTorch.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from ._build import build, lib_path  # noqa: F401
+
+__all__ = [
+    "FAError", "fa_fwd", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_version",
+    "attention", "load_library", "STATUS",
+]
+
+STATUS = {
+    0: "FA_OK", 1: "FA_ERR_NULL_PTR", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_BAD_SHAPE",
+    4: "FA_ERR_UNSUPPORTED_HEAD_DIM", 5: "FA_ERR_BAD_SCALE", 6: "FA_ERR_NO_DEVICE_SUPPORT",
+    7: "FA_ERR_LAUNCH", 8: "FA_ERR_DEVICE_TIMEOUT", 9: "FA_ERR_BAD_ARG", 10: "FA_ERR_BAD_POINTER",
+    11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA",
+}
+EXPORTED = ["fa_fwd", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_version"]
+
+
+class FAError(RuntimeError):
+    """A non-zero status from the library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        super().__init__(f"{where}: {self.name} ({fa_status_string(code)})")
+
+
+_LIB = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Loads the built library (once).  Raises if it is missing: there is no fallback."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    path = path or lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"attention library not built ({path}); run exact_io_aware_07_gb300.build()")
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_device_status.argtypes = [vp, ctypes.POINTER(i)]
+    lib.fa_device_status.restype = i
+    lib.fa_fwd_launch_shape.argtypes = [i, i, i, i, i, i] + [ctypes.POINTER(i)] * 3
+    lib.fa_fwd_launch_shape.restype = i
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = ctypes.c_char_p
+    if path == lib_path():
+        _LIB = lib
+    return lib
+
+
+def fa_status_string(code: int) -> str:
+    return load_library().fa_status_string(int(code)).decode()
+
+
+def fa_version() -> str:
+    return load_library().fa_version().decode()
+
+
+def fa_fwd_launch_shape(B: int, H: int, T: int, d: int, causal: bool, num_sms: int):
+    """(grid, threads, dynamic smem bytes) of the launch ``fa_fwd`` makes for these sizes."""
+    g, t, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    code = load_library().fa_fwd_launch_shape(B, H, T, d, int(causal), num_sms,
+                                              ctypes.byref(g), ctypes.byref(t), ctypes.byref(s))
+    if code:
+        raise FAError(code, "fa_fwd_launch_shape")
+    return g.value, t.value, s.value
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fa_device_status(stream=None) -> int:
+    """Reads and clears the device status word (0 = FA_OK, 8 = a wait ran out)."""
+    out = ctypes.c_int()
+    code = load_library().fa_device_status(ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(out))
+    if code:
+        raise FAError(code, "fa_device_status")
+    return out.value
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """O, LSE = attention(Q, K, V) into caller-owned tensors.
+
+    q, k, v, o: bf16 CUDA tensors (B, H, T, d), contiguous; lse: fp32 (B, H, T).
+    Enqueued on ``stream`` (default: PyTorch's current stream); not synchronised.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 (B, H, T, d) tensor")
+    if not (q.shape == k.shape == v.shape == o.shape):
+        raise ValueError("q, k, v and o must have the same shape")
+    B, H, T, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 (B, H, T) tensor")
+    lib = load_library()
+    code = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      B, H, T, d, int(bool(causal)), float(scale), ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_fwd")
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocates O (bf16) and LSE (fp32) and runs ``fa_fwd``; ``scale`` defaults to 1/sqrt(d)."""
+    import torch
+
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse

@@ -1,0 +1,240 @@
+// C ABI of the attention library: argument validation, TMA descriptors and the launch.
+// The operation and its contract are documented in include/fa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_kernel.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using PointerAttrFn = CUresult (*)(void*, CUpointer_attribute, CUdeviceptr);
+
+struct DriverFns {
+  EncodeTiledFn encode_tiled = nullptr;
+  PointerAttrFn pointer_attr = nullptr;
+};
+
+// Driver entry points, resolved through the runtime so the library needs no link to libcuda.
+const DriverFns& driver_fns() {
+  static DriverFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.encode_tiled = reinterpret_cast<EncodeTiledFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.pointer_attr = reinterpret_cast<PointerAttrFn>(f);
+  });
+  return fns;
+}
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s bound on any in-kernel wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int checked = 0;  // 0 unknown, 1 supported, -1 unsupported
+  int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mu;
+
+// The current device must be an sm_103 part; caches its SM count.
+fa_status current_device(int* dev_out, int* num_sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return FA_ERR_NO_DEVICE_SUPPORT;
+  }
+  if (dev >= kMaxDevices) return FA_ERR_NO_DEVICE_SUPPORT;
+  std::lock_guard<std::mutex> lock(g_devices_mu);
+  DeviceInfo& info = g_devices[dev];
+  if (info.checked == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    if (major == 10 && minor == 3) {
+      if (cudaSetDevice(dev) != cudaSuccess) {  // makes the primary context current
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+      }
+      info.num_sms = sms;
+      info.checked = 1;
+    } else {
+      info.checked = -1;
+    }
+  }
+  if (info.checked < 0) return FA_ERR_NO_DEVICE_SUPPORT;
+  *dev_out = dev;
+  *num_sms = info.num_sms;
+  return FA_OK;
+}
+
+// `p` must be device memory of device `dev`, and [p, p + bytes) must lie in one allocation.
+fa_status check_device_range(const void* p, size_t bytes, int dev) {
+  const DriverFns& fns = driver_fns();
+  if (!fns.pointer_attr) return FA_ERR_CUDA;
+  const CUdeviceptr dp = reinterpret_cast<CUdeviceptr>(p);
+  unsigned int mem_type = 0;
+  int ordinal = -1;
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  if (fns.pointer_attr(&mem_type, CU_POINTER_ATTRIBUTE_MEMORY_TYPE, dp) != CUDA_SUCCESS ||
+      mem_type != CU_MEMORYTYPE_DEVICE)
+    return FA_ERR_BAD_POINTER;
+  if (fns.pointer_attr(&ordinal, CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL, dp) != CUDA_SUCCESS || ordinal != dev)
+    return FA_ERR_BAD_POINTER;
+  if (fns.pointer_attr(&base, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS ||
+      fns.pointer_attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS)
+    return FA_ERR_BAD_POINTER;
+  if (dp < base || dp - base > size || bytes > size - (dp - base)) return FA_ERR_BAD_POINTER;
+  return FA_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Checks that need no device: pointers, sizes, head size, scale, mask flag, alignment.
+fa_status validate_host(const void* q, const void* k, const void* v, const void* o, const void* lse, int B, int H,
+                        int T, int d, int causal, float scale) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_PTR;
+  if (B < 1 || H < 1 || T < 1) return FA_ERR_BAD_SHAPE;
+  if (static_cast<long long>(B) * H > INT_MAX || T > (1 << 30)) return FA_ERR_BAD_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long nqb = (T + 255) / 256;
+  if (bh * nqb > INT_MAX) return FA_ERR_BAD_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_BAD_SCALE;
+  if (causal != 0 && causal != 1) return FA_ERR_BAD_ARG;
+  for (const void* p : {q, k, v, o, lse})
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
+  const DriverFns& fns = driver_fns();
+  if (!fns.encode_tiled) return false;
+  // 3-D view (d, T, B*H): a box never crosses from one head into the next, and
+  // rows past T read as zeros.
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(T) * d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return fns.encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int d,
+                 int causal, float scale, cudaStream_t stream) {
+  fa_status st = validate_host(q, k, v, o, lse, B, H, T, d, causal, scale);
+  if (st != FA_OK) return st;
+  int dev = 0, num_sms = 0;
+  if ((st = current_device(&dev, &num_sms)) != FA_OK) return st;
+
+  const int BH = B * H;
+  const size_t n_elem = static_cast<size_t>(BH) * T * d;
+  const size_t qkv_bytes = n_elem * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * T * 4;
+  for (const void* p : {q, k, v, static_cast<const void*>(o)})
+    if ((st = check_device_range(p, qkv_bytes, dev)) != FA_OK) return st;
+  if ((st = check_device_range(lse, lse_bytes, dev)) != FA_OK) return st;
+  for (const void* in : {q, k, v})
+    if (overlaps(o, qkv_bytes, in, qkv_bytes) || overlaps(lse, lse_bytes, in, qkv_bytes)) return FA_ERR_ALIAS;
+  if (overlaps(o, qkv_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
+
+  CUtensorMap tq, tk, tv;
+  if (!make_tensor_map(&tq, q, BH, T, d) || !make_tensor_map(&tk, k, BH, T, d) ||
+      !make_tensor_map(&tv, v, BH, T, d))
+    return FA_ERR_CUDA;
+
+  fa::Params p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = BH;
+  p.T = T;
+  p.causal = causal;
+  p.nqb = (T + 255) / 256;
+  p.nk = (T + 127) / 128;
+  p.num_units = BH * p.nqb;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.timeout_ns = kWaitLimitNs;
+  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
+  if (fa::launch_fa_fwd(d, tq, tk, tv, p, grid, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL_PTR: return "a required pointer is NULL";
+    case FA_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
+    case FA_ERR_BAD_SHAPE: return "B, H or T out of range";
+    case FA_ERR_UNSUPPORTED_HEAD_DIM: return "head size d must be 64 or 128";
+    case FA_ERR_BAD_SCALE: return "scale must be finite and > 0";
+    case FA_ERR_NO_DEVICE_SUPPORT: return "the current device is not an sm_103 GPU";
+    case FA_ERR_LAUNCH: return "kernel launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait ran out";
+    case FA_ERR_BAD_ARG: return "causal must be 0 or 1";
+    case FA_ERR_BAD_POINTER: return "a pointer is not device memory of the current device, or its allocation is too small";
+    case FA_ERR_ALIAS: return "an output overlaps an input or the other output";
+    case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+  }
+  return "unknown status";
+}
+
+fa_status fa_device_status(cudaStream_t stream, int* out) {
+  if (!out) return FA_ERR_NULL_PTR;
+  unsigned int word = 0;
+  if (fa::read_and_clear_status(stream, &word) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  *out = word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+  return FA_OK;
+}
+
+fa_status fa_fwd_launch_shape(int B, int H, int T, int d, int causal, int num_sms, int* grid, int* threads,
+                              int* smem_bytes) {
+  if (!grid || !threads || !smem_bytes) return FA_ERR_NULL_PTR;
+  static const char dummy[16] __attribute__((aligned(16))) = {};
+  fa_status st = validate_host(dummy, dummy, dummy, dummy, dummy, B, H, T, d, causal, 1.0f);
+  if (st != FA_OK) return st;
+  if (num_sms < 1) return FA_ERR_BAD_ARG;
+  const long long units = static_cast<long long>(B) * H * ((T + 255) / 256);
+  *grid = static_cast<int>(units < num_sms ? units : num_sms);
+  *threads = fa::fa_fwd_threads();
+  *smem_bytes = fa::fa_fwd_smem_bytes(d);
+  return FA_OK;
+}
+
+const char* fa_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,482 @@
+// FlashAttention forward for sm_103a: a warp-specialised persistent kernel.
+//
+// What it computes ("Flash Attention, tiled: exact attention without the T x T
+// HBM matrix", section "From the example to tiled GPU work", the per-tile
+// procedure; "FlashAttention: the IO-aware Attention Kernel", section 3.2):
+// for every query tile Q_i and every visible key/value tile K_j, V_j
+//   S_ij = Q_i K_j^T, masked; per row m' = max(m, max s), r = e^(m - m'),
+//   l = r l + sum p, o = r o + p^T V_j with p = e^(s - m'); at the end O = o / l
+// and the row's log-sum-exp.  Scores are kept in base-2 units of the scaled
+// score (s * scale * log2 e), so every exponential is one ex2.
+//
+// Lazy rescale ("FlashAttention and Fused Kernels", section "Four generations
+// of FlashAttention", FlashAttention-4): a row's reference max m is moved, and
+// l and o rescaled, only when the tile max exceeds m by more than log2(256) = 8;
+// otherwise the stale m is kept, so p <= 2^8, and the final o / l and the LSE
+// use that same m, which keeps the result exact up to rounding.
+//
+// Roles (320 threads, one CTA per SM, persistent over work units):
+//   warps 0-3  softmax for query tile 0 of the unit (one TMEM lane = one row per thread)
+//   warps 4-7  softmax for query tile 1
+//   warp 8     TMA producer: Q tiles once per unit, then K_j, V_j through a ring
+//   warp 9     TMEM allocator and tcgen05.mma issuer
+// A work unit is (batch*head, 256 query rows) = two 128-row query tiles that
+// share every K/V tile loaded.  Tensor Memory (512 columns):
+//   S_0 [0,128)  S_1 [128,256)  O_0 [256,256+d)  O_1 [256+d,256+2d)
+// P_i (bf16 pairs) is written over the first 64 columns of S_i once S_i has
+// been read; the MMA that next writes S_i is issued after the one reading P_i.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_kernel.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int BM = 128;          // query rows per tile
+constexpr int BN = 128;          // keys per tile
+constexpr int NUM_THREADS = 320;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16, 128-byte swizzle
+constexpr float LN2 = 0.693147180559945309f;
+
+__device__ unsigned int g_status;  // bit 0: a bounded wait ran out
+
+template <int D>
+struct Layout {
+  static constexpr int TILE_BYTES = BM * D * 2;
+  static constexpr int BOXES = D / 64;
+  static constexpr int STAGES = (D == 128) ? 4 : 8;
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = 2 * TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + STAGES * TILE_BYTES;
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2], done
+  static constexpr int NUM_BARS = 2 + 2 * STAGES + 8 + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // TMEM base slot, abort flag
+  // The V operand descriptor of the last ring stage may address up to 16 KB past a
+  // 128 x 64 tile (LBO, unused at N = 64); keep that range inside the allocation.
+  static constexpr int GUARD = (D == 64) ? 32 * 1024 : 0;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + GUARD + 1024;  // + slack to align the base to 1 KB
+  static __device__ __forceinline__ constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
+  static __device__ __forceinline__ constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * D; }
+};
+
+struct Unit {
+  int bh, qb;
+  int n[2];  // K/V tiles each query tile visits (0 = tile lies past T)
+};
+
+// Work unit w -> (batch*head, 256-row query block).  Causal launches take the
+// longest query blocks first so the persistent CTAs finish together.
+__device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
+  Unit u;
+  const int band = w / p.BH;
+  u.bh = w - band * p.BH;
+  u.qb = p.causal ? (p.nqb - 1 - band) : band;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int q0 = u.qb * 2 * BM + i * BM;
+    u.n[i] = (q0 >= p.T) ? 0 : (p.causal ? min(p.nk, q0 / BN + 1) : p.nk);
+  }
+  return u;
+}
+
+// Bounded mbarrier wait: gives up when another thread of the CTA has given up,
+// or after `limit_ns`; then it records the timeout and returns false.
+struct Waiter {
+  volatile int* abort_flag;
+  unsigned long long limit_ns;
+
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, true);
+  }
+  // Same, but keeps waiting after another thread gave up (used to drain work in flight).
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, false);
+  }
+  __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, bool honour_abort) const {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((it & 31u) == 0) {
+        if (honour_abort && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+          *abort_flag = 1;
+          atomicOr(&g_status, 1u);
+          return false;
+        }
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t q_smem = sbase + L::Q_OFF;
+  const uint32_t kv_smem = sbase + L::KV_OFF;
+  const uint32_t bar0 = sbase + L::BAR_OFF;
+  const uint32_t bar_q_full = bar0;
+  const uint32_t bar_q_empty = bar0 + 8;
+  auto bar_kv_full = [&](int s) { return bar0 + 16 + 8 * s; };
+  auto bar_kv_empty = [&](int s) { return bar0 + 16 + 8 * (L::STAGES + s); };
+  const uint32_t barx = bar0 + 16 + 16 * L::STAGES;
+  auto bar_s_full = [&](int i) { return barx + 8 * i; };
+  auto bar_p_full = [&](int i) { return barx + 16 + 8 * i; };
+  auto bar_o_full = [&](int i) { return barx + 32 + 8 * i; };
+  auto bar_o_empty = [&](int i) { return barx + 48 + 8 * i; };
+  const uint32_t bar_done = barx + 64;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_empty, 1);
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(bar_kv_full(s), 1);
+      mbar_init(bar_kv_empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_p_full(i), 4);
+      mbar_init(bar_o_full(i), 1);
+      mbar_init(bar_o_empty(i), 4);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter W{abort_flag, p.timeout_ns};
+
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int stage = 0;
+      uint32_t phase = 0, qe_phase = 0;
+      uint32_t issued = 0, issued_parity = 0, q_issued = 0, q_parity = 0;  // for draining after a timeout
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+        const Unit u = decode_unit(p, w);
+        const int nmax = max(u.n[0], u.n[1]);
+        if (!(ok = W.wait(bar_q_empty, qe_phase ^ 1))) break;
+        const int nq = (u.n[0] > 0) + (u.n[1] > 0);
+        mbar_arrive_expect_tx(bar_q_full, nq * L::TILE_BYTES);
+        for (int i = 0; i < 2; ++i) {
+          if (u.n[i] == 0) continue;
+          for (int b = 0; b < L::BOXES; ++b)
+            tma_load_3d(q_smem + i * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64, u.qb * 2 * BM + i * BM,
+                        u.bh, bar_q_full);
+        }
+        q_issued = 1;
+        q_parity = qe_phase;
+        qe_phase ^= 1;
+        for (int j = 0; ok && j < nmax; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!(ok = W.wait(bar_kv_empty(stage), phase ^ 1))) break;
+            mbar_arrive_expect_tx(bar_kv_full(stage), L::TILE_BYTES);
+            const CUtensorMap* tm = kv == 0 ? &tmK : &tmV;
+            for (int b = 0; b < L::BOXES; ++b)
+              tma_load_3d(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, tm, b * 64, j * BN, u.bh,
+                          bar_kv_full(stage));
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == L::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+      }
+      if (!ok) {  // let every copy already issued land before the CTA exits
+        if (q_issued) W.drain(bar_q_full, q_parity);
+        for (int s = 0; s < L::STAGES; ++s)
+          if (issued & (1u << s)) W.drain(bar_kv_full(s), (issued_parity >> s) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);   // S = Q K^T: both K-major
+      constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, D, 1);   // O += P V: V is MN-major
+      int stage = 0;
+      uint32_t phase = 0, qf_phase = 0;
+      uint32_t pf_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
+      bool ok = true;
+      auto take = [&](int& s_out) -> bool {  // the next filled ring slot
+        s_out = stage;
+        if (!W.wait(bar_kv_full(stage), phase)) return false;
+        if (++stage == L::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+        tc_fence_after();
+        return true;
+      };
+      auto issue_s = [&](int i, int ks) {  // S_i = Q_i K^T over d in steps of 16
+        const uint32_t qa = q_smem + i * L::TILE_BYTES;
+        const uint32_t ka = kv_smem + ks * L::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * BOX_BYTES + (kk % 4) * 32;
+          mma_ss(tmem + L::s_col(i), make_sdesc_sw128(qa + off, 16, 1024), make_sdesc_sw128(ka + off, 16, 1024),
+                 IDESC_S, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int i, int vs, bool acc) {  // O_i (+)= P_i V over keys in steps of 16
+        const uint32_t va = kv_smem + vs * L::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + L::o_col(i), tmem + L::s_col(i) + kk * 8, make_sdesc_sw128(va + kk * 2048, BOX_BYTES, 1024),
+                 IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+      };
+      for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+        const Unit u = decode_unit(p, w);
+        const int n0 = u.n[0], n1 = u.n[1], nmax = max(n0, n1);
+        const int last_i = n1 > 0 ? 1 : 0;
+        if (!(ok = W.wait(bar_q_full, qf_phase))) break;
+        qf_phase ^= 1;
+        tc_fence_after();
+        int ks;
+        if (!(ok = take(ks))) break;
+        for (int i = 0; i < 2; ++i) {
+          if (u.n[i] == 0) continue;
+          issue_s(i, ks);
+          mma_commit(bar_s_full(i));
+          if (i == last_i && u.n[i] == 1) mma_commit(bar_q_empty);
+        }
+        mma_commit(bar_kv_empty(ks));
+        for (int j = 0; ok && j < nmax; ++j) {
+          int vs;
+          if (!(ok = take(vs))) break;
+          int ks1 = -1;
+          if (j < n0) {
+            if (j == 0) {
+              if (!(ok = W.wait(bar_o_empty(0), oe_phase[0] ^ 1))) break;
+              oe_phase[0] ^= 1;
+            }
+            if (!(ok = W.wait(bar_p_full(0), pf_phase[0]))) break;
+            pf_phase[0] ^= 1;
+            tc_fence_after();
+            issue_pv(0, vs, j > 0);
+            if (j + 1 == n0) mma_commit(bar_o_full(0));
+            if (j + 1 < n0) {
+              if (!(ok = take(ks1))) break;
+              issue_s(0, ks1);
+              mma_commit(bar_s_full(0));
+              if (last_i == 0 && j + 2 == n0) mma_commit(bar_q_empty);
+            }
+          }
+          if (j < n1) {
+            if (j == 0) {
+              if (!(ok = W.wait(bar_o_empty(1), oe_phase[1] ^ 1))) break;
+              oe_phase[1] ^= 1;
+            }
+            if (!(ok = W.wait(bar_p_full(1), pf_phase[1]))) break;
+            pf_phase[1] ^= 1;
+            tc_fence_after();
+            issue_pv(1, vs, j > 0);
+            if (j + 1 == n1) mma_commit(bar_o_full(1));
+          }
+          mma_commit(bar_kv_empty(vs));
+          if (j + 1 < n1) {
+            if (ks1 < 0 && !(ok = take(ks1))) break;
+            issue_s(1, ks1);
+            mma_commit(bar_s_full(1));
+            if (j + 2 == n1) mma_commit(bar_q_empty);
+          }
+          if (ks1 >= 0) mma_commit(bar_kv_empty(ks1));
+        }
+      }
+      // every MMA and every commit arrival has landed before TMEM is freed
+      mma_commit(bar_done);
+      W.drain(bar_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int i = warp / 4;        // query tile of this warpgroup
+    const int wq = warp % 4;       // TMEM lane quarter this warp may access
+    const int rt = wq * 32 + lane;  // row within the query tile
+    const uint32_t lane_off = uint32_t(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + L::s_col(i);
+    const uint32_t t_o = tmem + lane_off + L::o_col(i);
+    const float sl2 = p.scale_log2;
+    uint32_t sf_phase = 0, of_phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+      const Unit u = decode_unit(p, w);
+      const int n = u.n[i];
+      if (n == 0) continue;
+      const int q0 = u.qb * 2 * BM + i * BM;
+      const int row = q0 + rt;
+      float m_run = -INFINITY;  // reference max, base-2 units of the scaled score
+      float l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        if (!(ok = W.wait(bar_s_full(i), sf_phase))) break;
+        sf_phase ^= 1;
+        tc_fence_after();
+        uint32_t sr[BN];
+        tmem_ld128_wait(t_s, sr);
+        const int k0 = j * BN;
+        if ((p.causal && k0 + BN - 1 > q0) || k0 + BN > p.T) {  // diagonal or ragged tail tile
+          int lim = p.T - k0;
+          if (p.causal) lim = min(lim, row - k0 + 1);
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= lim) sr[c] = f2u(-INFINITY);
+        }
+        float m4[4] = {u2f(sr[0]), u2f(sr[1]), u2f(sr[2]), u2f(sr[3])};
+#pragma unroll
+        for (int c = 4; c < BN; c += 8)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m4[e] = max3f(m4[e], u2f(sr[c + 2 * e]), u2f(sr[c + 2 * e + 1]));
+        float mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+        mx *= sl2;
+        // lazy rescale decision (warp-uniform: TMEM access below is warp-collective)
+        float r = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_run = mx;
+        } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
+          const float m_new = (mx > m_run + 8.f) ? mx : m_run;
+          r = ex2_approx(m_run - m_new);
+          m_run = m_new;
+          l *= r;
+          rescale = true;
+        }
+        const float nm = -m_run;
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(fmaf(u2f(sr[32 * c + 2 * e]), sl2, nm));
+            const float p1 = ex2_approx(fmaf(u2f(sr[32 * c + 2 * e + 1]), sl2, nm));
+            l0 += p0;
+            l1 += p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(t_s + c * 16, pk);
+        }
+        l += l0 + l1;
+        if (rescale) {  // o *= r; PV_i(j-1) has completed (it was issued before S_i(j))
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32_wait(t_o + c * 32, ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = f2u(u2f(ov[e]) * r);
+            tmem_st32(t_o + c * 32, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p_full(i));
+      }
+      if (!ok) break;
+      // epilogue: O = o / l in bf16, LSE = ln(2) (m + log2 l)
+      if (!(ok = W.wait(bar_o_full(i), of_phase))) break;
+      of_phase ^= 1;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(u.bh) * p.T + row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32_wait(t_o + c * 32, ov);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(ov[2 * e]) * inv_l, u2f(ov[2 * e + 1]) * inv_l);
+        if (row < p.T) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+      if (row < p.T) p.lse[static_cast<size_t>(u.bh) * p.T + row] = (m_run + log2f(l)) * LN2;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_o_empty(i));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+template <int D>
+static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
+                          int grid, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Layout<D>::SMEM_BYTES;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D>, q, k, v, p);
+}
+
+cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const Params& p, int grid, cudaStream_t stream) {
+  if (d == 64) return launch<64>(q, k, v, p, grid, stream);
+  return launch<128>(q, k, v, p, grid, stream);
+}
+
+int fa_fwd_smem_bytes(int d) { return d == 64 ? Layout<64>::SMEM_BYTES : Layout<128>::SMEM_BYTES; }
+int fa_fwd_threads() { return NUM_THREADS; }
+int fa_fwd_rows_per_unit() { return 2 * BM; }
+
+cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* out) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace fa

@@ -1,0 +1,29 @@
+// Internal interface between the C-ABI layer (fa_api.cu) and the kernel (fa_kernel.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+struct Params {
+  __nv_bfloat16* o;           // (B*H, T, d) bf16 output
+  float* lse;                 // (B*H, T) fp32 output
+  int BH;                     // batch * heads
+  int T;                      // sequence length
+  int causal;                 // 0 or 1
+  int nqb;                    // 256-row query blocks per head: ceil(T / 256)
+  int nk;                     // 128-key tiles per head: ceil(T / 128)
+  int num_units;              // BH * nqb
+  float scale_log2;           // scale * log2(e)
+  unsigned long long timeout_ns;  // bound on every in-kernel wait
+};
+
+cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const Params& p, int grid, cudaStream_t stream);
+int fa_fwd_smem_bytes(int d);
+int fa_fwd_threads();
+int fa_fwd_rows_per_unit();
+cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* out);
+
+}  // namespace fa

@@ -1,0 +1,103 @@
+/*
+ * fa.h - FlashAttention forward pass for one GB300 (sm_103), C ABI.
+ *
+ * The operation (exact attention, tiled, with the online softmax):
+ *   for every batch b, head h and query row i,
+ *     s_ij  = scale * sum_c Q[b,h,i,c] * K[b,h,j,c]      for visible keys j
+ *     O[b,h,i,:] = sum_j softmax_j(s_i.) * V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp(s_ij)                      (natural log)
+ *   where key j is visible to query i when causal == 0, or when j <= i if
+ *   causal == 1.
+ * Sources: "Flash Attention, tiled: exact attention without the T x T HBM
+ * matrix", sections "Ordinary causal attention" (S = Q K^T / sqrt(d), causal
+ * mask, softmax, Y = P V) and "From the example to tiled GPU work" (the
+ * per-tile procedure and its outputs: the output and limited softmax state);
+ * "FlashAttention and Fused Kernels: Attention Without the n x n Matrix",
+ * section "Step 3: FlashAttention, one fused kernel"; "FlashAttention: the
+ * IO-aware Attention Kernel", section 3.2 (the online-softmax recurrence).
+ * The LSE is not defined on the pages; this library writes the natural log of
+ * the softmax denominator of the scaled, masked scores.
+ *
+ * Memory layout: Q, K, V and O are dense, contiguous, row-major bf16 tensors
+ * of shape (B, H, T, d) (d fastest).  LSE is a dense fp32 tensor (B, H, T).
+ *
+ * Ownership: the caller owns every buffer; all five pointers are device
+ * memory of the current CUDA device.  The library allocates no memory and
+ * keeps no per-call state.  O and LSE must not overlap Q, K, V or each other.
+ *
+ * Execution: fa_fwd only validates its arguments and enqueues one kernel on
+ * `stream`; it does not synchronise.  O and LSE are complete once the stream
+ * has reached that point.
+ *
+ * Errors: validation happens before anything is enqueued and returns a status
+ * code other than FA_OK; nothing is written in that case.  Every wait inside
+ * the kernel is bounded in time: if one runs out, the kernel stops early,
+ * records FA_ERR_DEVICE_TIMEOUT in a device status word and returns, leaving
+ * O and LSE incomplete; fa_device_status() reads (and clears) that word.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL_PTR = 1,              /* a required pointer is NULL */
+  FA_ERR_MISALIGNED = 2,            /* a pointer is not 16-byte aligned */
+  FA_ERR_BAD_SHAPE = 3,             /* B, H or T < 1, or a size too large to index */
+  FA_ERR_UNSUPPORTED_HEAD_DIM = 4,  /* d is not 64 or 128 */
+  FA_ERR_BAD_SCALE = 5,             /* scale is not finite and > 0 */
+  FA_ERR_NO_DEVICE_SUPPORT = 6,     /* the current device is not sm_103 */
+  FA_ERR_LAUNCH = 7,                /* the CUDA runtime refused the launch */
+  FA_ERR_DEVICE_TIMEOUT = 8,        /* a bounded in-kernel wait ran out */
+  FA_ERR_BAD_ARG = 9,               /* causal is not 0 or 1 */
+  FA_ERR_BAD_POINTER = 10,          /* a pointer is not device memory, or its allocation is too small */
+  FA_ERR_ALIAS = 11,                /* O or LSE overlaps an input or each other */
+  FA_ERR_CUDA = 12                  /* a CUDA runtime or driver query failed */
+} fa_status;
+
+/*
+ * Attention forward.
+ *   q, k, v : bf16 (B, H, T, d), contiguous, read only.
+ *   o       : bf16 (B, H, T, d), contiguous, written: O = softmax(scale Q K^T [+ mask]) V.
+ *   lse     : fp32 (B, H, T), written: natural-log LSE of each row's scaled scores.
+ *   B, H, T : batch, heads, sequence length; each >= 1; B*H <= 2^31-1, T <= 2^30.
+ *   d       : head size, 64 or 128.
+ *   causal  : 1 = query i sees keys j <= i; 0 = every key.
+ *   scale   : score multiplier, finite and > 0 (usually 1/sqrt(d)).
+ *   stream  : CUDA stream the kernel is enqueued on (0 = legacy default).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int T, int d, int causal, float scale,
+                 cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Reads and clears the device status word that kernels of this library set
+ * when a bounded wait runs out.  Synchronises `stream` first.  *out receives
+ * FA_OK or FA_ERR_DEVICE_TIMEOUT.  Returns FA_ERR_CUDA if the copy fails.
+ */
+fa_status fa_device_status(cudaStream_t stream, int* out);
+
+/*
+ * The launch the library would make for these sizes: persistent CTAs, threads
+ * per CTA and dynamic shared memory bytes.  For tools and tests; it validates
+ * d and the sizes like fa_fwd but needs no device pointers.
+ */
+fa_status fa_fwd_launch_shape(int B, int H, int T, int d, int causal, int num_sms,
+                              int* grid, int* threads, int* smem_bytes);
+
+/* Library version, e.g. "0.1.0". */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

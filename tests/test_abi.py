@@ -1,0 +1,93 @@
+"""The C-ABI library: it builds, loads, exports every declared symbol, and validates on the host.
+
+No test here launches a kernel; they run without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_io_aware_07_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_]+\s*\*?\s*(fa_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def _declared_status_codes():
+    text = open(HEADER).read()
+    return {int(v): k for k, v in re.findall(r"(FA_[A-Z_]+)\s*=\s*(\d+)", text)}
+
+
+def test_header_declares_the_entry_points():
+    assert _declared_functions() == sorted(fa.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    # exported with C linkage (no C++ mangling) in the dynamic symbol table
+    out = os.popen(f"nm -D --defined-only {fa.lib_path()}").read()
+    for name in _declared_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_status_codes_match_header(lib):
+    assert _declared_status_codes() == fa.STATUS
+    for code in fa.STATUS:
+        assert fa.fa_status_string(code) and "unknown" not in fa.fa_status_string(code)
+    assert "unknown" in fa.fa_status_string(99)
+
+
+def test_version(lib):
+    assert re.match(r"^\d+\.\d+\.\d+$", fa.fa_version())
+
+
+A = 0x10000  # fake, 16-byte-aligned addresses: validation fails before any is touched
+
+
+def _call(lib, q=A, k=A + 0x1000, v=A + 0x2000, o=A + 0x3000, lse=A + 0x4000,
+          B=1, H=2, T=128, d=64, causal=0, scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, T, d, causal, ctypes.c_float(scale), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(k=0), 1), (dict(v=0), 1), (dict(o=0), 1), (dict(lse=0), 1),
+    (dict(B=0), 3), (dict(H=0), 3), (dict(T=0), 3), (dict(T=-5), 3), (dict(T=(1 << 30) + 1), 3),
+    (dict(B=1 << 16, H=1 << 16), 3),
+    (dict(d=96), 4), (dict(d=0), 4), (dict(d=256), 4),
+    (dict(scale=0.0), 5), (dict(scale=-1.0), 5), (dict(scale=float("nan")), 5), (dict(scale=float("inf")), 5),
+    (dict(causal=2), 9), (dict(causal=-1), 9),
+    (dict(q=A + 8), 2), (dict(o=A + 0x3004), 2), (dict(lse=A + 0x4002), 2),
+])
+def test_host_validation(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+def test_valid_arguments_reach_the_device_checks(lib):
+    # every host check passes; without a GPU the device check refuses, with one the
+    # fake addresses are refused as non-device memory; nothing is launched either way
+    assert _call(lib) in (6, 10)
+
+
+def test_launch_shape(lib):
+    assert fa.fa_fwd_launch_shape(1, 4, 256, 64, True, 152)[0] == 4       # 4 units of 256 rows
+    assert fa.fa_fwd_launch_shape(8, 12, 1024, 64, True, 152)[0] == 152   # 384 units, capped at the SMs
+    g, t, s = fa.fa_fwd_launch_shape(1, 32, 4096, 128, False, 152)
+    assert (g, t) == (152, 320) and 128 * 1024 < s <= 232_448
+    g, t, s = fa.fa_fwd_launch_shape(1, 1, 1, 64, False, 152)
+    assert g == 1 and s <= 232_448
+    with pytest.raises(fa.FAError):
+        fa.fa_fwd_launch_shape(1, 1, 128, 80, False, 152)
