@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Attention forward throughput on one GB300 (or N replicas), printed as one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one FlashAttention forward pass (the whole hot path: one kernel)
+over one batch of the workload.  ``value`` is the attention-forward rate in
+TFLOPS with FLOPs = 4 B H T^2 d, halved for a causal mask, inputs resident in
+HBM.  Between timed steps the inputs rotate over enough copies that their
+total exceeds twice the L2, so no step starts with its operands in L2.
+``e2e`` is the same metric through the public Python API with pinned host
+buffers: every step copies Q, K, V in and O, LSE out inside the timed region.
+
+``--impl reference`` times the float64 CPU oracle (the slow, plain
+definition) on the host cores instead, on a bounded sample of the same
+workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import fa_inputs as fi  # noqa: E402
+
+DEFAULT_WORKLOAD = "gpt2s_causal_b8h12t1024d64"
+METRIC = "attention fwd TFLOPS (bf16, 1 GB300) and % of dense BF16 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+SWEEP_DEFAULT = ["tiny_causal_b1h4t256d64", "gpt2m_b16h16t1024d64", "gpt2m_stress_b16h16t1024d64",
+                 "llama8b_causal_b1h32t4096d128", "llama8b_b1h32t4096d128", "long_causal_b1h32t32768d128"]
+
+
+def metric_flops(B, H, T, d, causal):
+    f = 4.0 * B * H * T * T * d
+    return f / 2 if causal else f
+
+
+def floor_bytes(B, H, T, d):
+    """Read Q, K, V once and write O (bf16) and LSE (fp32) once."""
+    return 4 * B * H * T * d * 2 + B * H * T * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def library_fingerprint():
+    from exact_io_aware_07_gb300 import _build
+
+    return _build._fingerprint(())[:16]
+
+
+def recorded_traffic(workload, fingerprint):
+    """DRAM bytes per launch from an ncu summary under profiles/, if taken on this kernel build."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    pat = re.compile(rf"^traffic_bytes_per_launch\s+{re.escape(workload)}\s+(\d+)\s+fingerprint\s+(\w+)", re.M)
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for m in pat.finditer(f.read()):
+                if m.group(2) == fingerprint:
+                    return int(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons while the GPU works."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in use for k, v in enumerate(r[4]) if v.lower().startswith("active")})
+        return {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": max(r[2] for r in use),
+                "power_w_max": max(r[3] for r in use), "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": len(inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")  # host-side barrier and timing reduction only
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x):
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def device_inputs(qkv, torch, dev):
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    return up(qkv.q_bits), up(qkv.k_bits), up(qkv.v_bits)
+
+
+def time_kernel(fa, torch, dev, w, qkv, steps, warmup, scale, per_step_events=True):
+    """Device-timed steps over rotating input copies; returns (total_s, per-launch mean s, nsets)."""
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    q0, k0, v0 = device_inputs(qkv, torch, dev)
+    set_bytes = 4 * q0.numel() * 2 + B * H * T * 4
+    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes)) if set_bytes < 2 * L2_BYTES else 1
+    sets = []
+    for s in range(nsets):
+        q, k, v = (q0, k0, v0) if s == 0 else (q0.clone(), k0.clone(), v0.clone())
+        sets.append((q, k, v, torch.empty_like(q), torch.empty((B, H, T), dtype=torch.float32, device=dev)))
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        q, k, v, o, lse = sets[i % nsets]
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)] \
+        if per_step_events else []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    return sets, stream, ev, start, end, nsets
+
+
+def run_ours(args, world, rank, local, pg):
+    import torch
+
+    import exact_io_aware_07_gb300 as fa
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.build()
+    fa.load_library()
+    name = args.workload
+    w = fi.WORKLOADS[name]
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    scale = 1.0 / math.sqrt(d)
+    peaks, peak_src = load_peaks()
+    qkv = fi.make_qkv(B, H, T, d, seed=0, sigma_qk=w["sigma_qk"])
+    K, W = args.steps, args.warmup
+    per_step = K <= 50000
+    sets, stream, ev, start, end, nsets = time_kernel(fa, torch, dev, w, qkv, K, W, scale, per_step)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        q, k, v, o, lse = sets[i % nsets]
+        if per_step:
+            ev[i][0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
+        if per_step:
+            ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(pg)
+    clk = clocks.stop(t_wall0, t_wall1)
+    total_s = start.elapsed_time(end) / 1e3
+    launch_s = (sum(a.elapsed_time(b) for a, b in ev) / 1e3 / K) if per_step else total_s / K
+    if fa.fa_device_status(stream) != 0:
+        raise RuntimeError("a bounded in-kernel wait ran out during the timed region")
+    total_s = max_over_ranks(pg, total_s)
+    launch_s = max_over_ranks(pg, launch_s)
+
+    f_step = metric_flops(B, H, T, d, causal)
+    value = world * K * f_step / total_s / 1e12
+    achieved = f_step / launch_s / 1e12
+    fp = library_fingerprint()
+    roofline = {
+        "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": recorded_traffic(name, fp),
+        "peak_source": f"{peak_src} bf16 burst", "kernel": "fa_fwd_kernel",
+        "floor_bytes": floor_bytes(B, H, T, d),
+        "attainable_tflops": round(min(peaks["bf16_tflops"],
+                                       f_step / floor_bytes(B, H, T, d) * peaks["hbm_gbs"] / 1e3), 1),
+        "hbm_floor_gbs": round(floor_bytes(B, H, T, d) / launch_s / 1e9, 1),
+    }
+
+    e2e = run_e2e(fa, torch, dev, w, qkv, scale, min(K, args.e2e_steps), pg) if not args.no_e2e else None
+    if e2e is not None:
+        e2e["value"] = round(world * e2e.pop("steps") * f_step / e2e.pop("seconds") / 1e12, 3)
+
+    sweep = None
+    if rank == 0 and world == 1 and not args.no_sweep:
+        sweep = run_sweep(fa, torch, dev, [s for s in args.sweep.split(",") if s and s != name], peaks)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, qkv, scale, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(total_s / K * 1e3, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "H": H, "T": T, "d": d, "causal": bool(causal),
+                   "scale": scale, "qkv_dist": f"Q,K~N(0,{w['sigma_qk']}^2), V~N(0,1), bf16, seed 0",
+                   "l2": f"inputs rotate over {nsets} copies ({nsets * 4 * B * H * T * d * 2 / 1e6:.0f} MB > 2x L2)"
+                         if nsets > 1 else "one input set larger than 2x L2",
+                   "parallelism": f"replicas x{world}", "flops_per_step": f_step},
+        "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+        "roofline": roofline, "e2e": e2e, "gpu_launches": K, "clocks": clk, "cpu_baseline": cpu,
+        "library_fingerprint": fp,
+    }
+    if sweep is not None:
+        line["sweep"] = sweep
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(fa, torch, dev, w, qkv, scale, steps, pg):
+    """Public API with pinned host buffers: H2D of Q, K, V and D2H of O, LSE inside every timed step."""
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+
+    def pinned(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    qh, kh, vh = pinned(qkv.q_bits), pinned(qkv.k_bits), pinned(qkv.v_bits)
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.empty(qh.shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        o, lse = fa.attention(qd, kd, vd, causal=bool(causal), scale=scale, stream=stream)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    sec = max_over_ranks(pg, a.elapsed_time(b) / 1e3)
+    return {"unit": "TFLOPS", "steps": steps, "seconds": sec,
+            "h2d_bytes_per_step": 3 * qh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
+            "path": "exact_io_aware_07_gb300.attention() with pinned host buffers"}
+
+
+def run_sweep(fa, torch, dev, names, peaks):
+    """Every other workload, measured the same way with fewer steps (informational)."""
+    out = {}
+    for name in names:
+        w = fi.WORKLOADS[name]
+        B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+        scale = 1.0 / math.sqrt(d)
+        qkv = fi.make_qkv(B, H, T, d, seed=0, sigma_qk=w["sigma_qk"])
+        f = metric_flops(B, H, T, d, causal)
+        steps = int(min(2000, max(20, 0.5 / max(f / 1.0e15, 1e-6))))
+        sets, stream, ev, start, end, nsets = time_kernel(fa, torch, dev, w, qkv, steps, 5, scale, True)
+        for i in range(steps):
+            q, k, v, o, lse = sets[i % nsets]
+            ev[i][0].record(stream)
+            fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        ms = sorted(a.elapsed_time(b) for a, b in ev)
+        mean_s = sum(ms) / len(ms) / 1e3
+        out[name] = {"ms_mean": round(mean_s * 1e3, 4), "ms_median": round(ms[len(ms) // 2], 4),
+                     "tflops": round(f / mean_s / 1e12, 1),
+                     "pct_of_bf16_peak": round(100 * f / mean_s / 1e12 / peaks["bf16_tflops"], 1),
+                     "steps": steps}
+        del sets
+        torch.cuda.empty_cache()
+    return out
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = max((i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"), default=0)
+        if n:
+            return n
+    except ImportError:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(w, qkv, scale, seconds):
+    """The float64 oracle, as it stands, on heads of the same input until ~`seconds` of CPU work."""
+    import oracle
+
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    q, k, v = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    rows_per_block = T if T <= 4096 else 256
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    done_rows = 0
+    t0 = time.perf_counter()
+    it = 0
+    while True:
+        b, h = heads[it % len(heads)]
+        r0 = (it // len(heads)) * rows_per_block % T
+        rows = np.arange(r0, min(T, r0 + rows_per_block))
+        oracle.attention_head(q[b, h], k[b, h], v[b, h], causal, scale, rows=rows)
+        done_rows += len(rows)
+        it += 1
+        if time.perf_counter() - t0 >= seconds or done_rows >= 4 * B * H * T:
+            break
+    dt = time.perf_counter() - t0
+    f = metric_flops(1, 1, T, d, causal) / T * done_rows  # metric FLOPs of the rows evaluated
+    return {"value": round(f / dt / 1e12, 6), "unit": "TFLOPS", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{done_rows} query rows ({done_rows / (B * H * T):.3f} of the workload) in "
+                      f"{rows_per_block}-row blocks, {dt:.1f} s, float64 numpy"}
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle timed per step on a bounded sample of the workload (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+
+    name = args.workload
+    w = fi.WORKLOADS[name]
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    scale = 1.0 / math.sqrt(d)
+    qkv = fi.make_qkv(B, H, T, d, seed=0, sigma_qk=w["sigma_qk"])
+    q, k, v = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    K, W = args.steps, args.warmup
+    # rows per step so that the whole run stays within about `budget` seconds
+    t0 = time.perf_counter()
+    oracle.attention_head(q[0, 0], k[0, 0], v[0, 0], causal, scale, rows=np.arange(min(T, 64)))
+    per_row = (time.perf_counter() - t0) / min(T, 64)
+    rows = int(max(1, min(T, args.reference_budget / max(K + W, 1) / max(per_row, 1e-9))))
+    heads = [(b, h) for b in range(B) for h in range(H)]
+
+    def step(i):
+        b, h = heads[i % len(heads)]
+        r0 = (i // len(heads)) * rows % T
+        rr = np.arange(r0, min(T, r0 + rows))
+        oracle.attention_head(q[b, h], k[b, h], v[b, h], causal, scale, rows=rr)
+        return len(rr)
+
+    for i in range(W):
+        step(i)
+    t0 = time.perf_counter()
+    n_rows = sum(step(W + i) for i in range(K))
+    dt = time.perf_counter() - t0
+    f = metric_flops(1, 1, T, d, causal) / T * n_rows
+    value = f / dt / 1e12
+    sample = f"{rows} query rows of one head per step ({n_rows} rows in {K} steps), float64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(dt / K * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "B": B, "H": H, "T": T, "d": d, "causal": bool(causal), "scale": scale},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": oracle_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fi.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep", default=",".join(SWEEP_DEFAULT))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-budget", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local, pg = dist_setup()
+    if args.gpus != world and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

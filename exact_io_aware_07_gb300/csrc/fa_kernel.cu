@@ -15,6 +15,12 @@
 // otherwise the stale m is kept, so p <= 2^8, and the final o / l and the LSE
 // use that same m, which keeps the result exact up to rounding.
 //
+// Two row sums are kept: lr sums the bf16-rounded weights p~ that the P V MMA
+// multiplies by, and O = sum p~ v / lr is a convex combination of the value
+// rows under exactly the weights used (a row dominated by one key returns that
+// key's value row unchanged, whatever the stale m); l sums the fp32 weights and
+// gives the LSE without the bf16 rounding of the weights.
+//
 // Roles (320 threads, one CTA per SM, persistent over work units):
 //   warps 0-3  softmax for query tile 0 of the unit (one TMEM lane = one row per thread)
 //   warps 4-7  softmax for query tile 1
@@ -338,7 +344,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const int q0 = u.qb * 2 * BM + i * BM;
       const int row = q0 + rt;
       float m_run = -INFINITY;  // reference max, base-2 units of the scaled score
-      float l = 0.f;
+      float l = 0.f;            // sum of the fp32 weights: the softmax denominator of the LSE
+      float lr = 0.f;           // sum of the bf16 weights the P V product used: divides O
       for (int j = 0; j < n; ++j) {
         if (!(ok = W.wait(bar_s_full(i), sf_phase))) break;
         sf_phase ^= 1;
@@ -353,9 +360,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           for (int c = 0; c < BN; ++c)
             if (c >= lim) sr[c] = f2u(-INFINITY);
         }
-        float m4[4] = {u2f(sr[0]), u2f(sr[1]), u2f(sr[2]), u2f(sr[3])};
+        float m4[4];  // four independent max chains over columns 0-7, then 8 columns per step
 #pragma unroll
-        for (int c = 4; c < BN; c += 8)
+        for (int e = 0; e < 4; ++e) m4[e] = fmaxf(u2f(sr[2 * e]), u2f(sr[2 * e + 1]));
+#pragma unroll
+        for (int c = 8; c < BN; c += 8)
 #pragma unroll
           for (int e = 0; e < 4; ++e) m4[e] = max3f(m4[e], u2f(sr[c + 2 * e]), u2f(sr[c + 2 * e + 1]));
         float mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
@@ -370,10 +379,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           r = ex2_approx(m_run - m_new);
           m_run = m_new;
           l *= r;
+          lr *= r;
           rescale = true;
         }
         const float nm = -m_run;
-        float l0 = 0.f, l1 = 0.f;
+        float l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -384,10 +394,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             l0 += p0;
             l1 += p1;
             pk[e] = pack_bf16x2(p0, p1);
+            add_bf16x2_f32(pk[e], lr0, lr1);
           }
           tmem_st16(t_s + c * 16, pk);
         }
         l += l0 + l1;
+        lr += lr0 + lr1;
         if (rescale) {  // o *= r; PV_i(j-1) has completed (it was issued before S_i(j))
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -408,7 +420,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (!(ok = W.wait(bar_o_full(i), of_phase))) break;
       of_phase ^= 1;
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(u.bh) * p.T + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

@@ -180,4 +180,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return y;
 }
 
+// acc_lo += low bf16 half of `packed`, acc_hi += high half (mixed-precision adds, fp32 result).
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t packed, float& acc_lo, float& acc_hi) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi) : "r"(packed));
+}
+
 }  // namespace fa
