@@ -55,40 +55,39 @@ template <int D>
 struct Layout {
   static constexpr int TILE_BYTES = BM * D * 2;
   static constexpr int BOXES = D / 64;
-  static constexpr int STAGES = (D == 128) ? 4 : 8;
-  static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = 2 * TILE_BYTES;
+  static constexpr int STAGES = (D == 128) ? 3 : 6;   // K/V ring depth (tiles)
+  static constexpr int Q_OFF = 0;                      // 2 units x 2 query tiles (double-buffered)
+  static constexpr int KV_OFF = 4 * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + STAGES * TILE_BYTES;
-  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2], done
-  static constexpr int NUM_BARS = 2 + 2 * STAGES + 8 + 1;
+  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2], done
+  static constexpr int NUM_BARS = 4 + 2 * STAGES + 8 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // TMEM base slot, abort flag
-  // The V operand descriptor of the last ring stage may address up to 16 KB past a
-  // 128 x 64 tile (LBO, unused at N = 64); keep that range inside the allocation.
-  static constexpr int GUARD = (D == 64) ? 32 * 1024 : 0;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + GUARD + 1024;  // + slack to align the base to 1 KB
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
   static __device__ __forceinline__ constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
   static __device__ __forceinline__ constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * D; }
 };
 
 struct Unit {
   int bh, qb;
-  int n[2];  // K/V tiles each query tile visits (0 = tile lies past T)
+  int n0, n1;  // K/V tiles each query tile visits (0 = the tile lies past T)
 };
 
-// Work unit w -> (batch*head, 256-row query block).  Causal launches take the
-// longest query blocks first so the persistent CTAs finish together.
+// Work item w -> (batch*head, 256-row query block).  Causal launches list the
+// longest query blocks first.
 __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
   Unit u;
   const int band = w / p.BH;
   u.bh = w - band * p.BH;
   u.qb = p.causal ? (p.nqb - 1 - band) : band;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int q0 = u.qb * 2 * BM + i * BM;
-    u.n[i] = (q0 >= p.T) ? 0 : (p.causal ? min(p.nk, q0 / BN + 1) : p.nk);
-  }
+  const int q0 = u.qb * 2 * BM, q1 = q0 + BM;
+  u.n0 = (q0 >= p.T) ? 0 : (p.causal ? min(p.nk, q0 / BN + 1) : p.nk);
+  u.n1 = (q1 >= p.T) ? 0 : (p.causal ? min(p.nk, q1 / BN + 1) : p.nk);
   return u;
 }
+
+// The k-th work item of CTA b in a grid of G: a snake over the heavy-first list
+// (b, 2G-1-b, 2G+b, ...), which pairs long causal units with short ones.
+__device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k & 1) ? (G - 1 - b) : b); }
 
 // Bounded mbarrier wait: gives up when another thread of the CTA has given up,
 // or after `limit_ns`; then it records the timeout and returns false.
@@ -105,7 +104,7 @@ struct Waiter {
     if (mbar_try_wait(bar, parity)) return true;
     return wait_slow(bar, parity, false);
   }
-  __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, bool honour_abort) const {
+  __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, bool honour_abort) const {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
       if (mbar_try_wait(bar, parity)) return true;
@@ -132,37 +131,41 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t q_smem = sbase + L::Q_OFF;
+  const uint32_t q_smem = sbase + L::Q_OFF;   // [unit buffer][query tile]
   const uint32_t kv_smem = sbase + L::KV_OFF;
   const uint32_t bar0 = sbase + L::BAR_OFF;
-  const uint32_t bar_q_full = bar0;
-  const uint32_t bar_q_empty = bar0 + 8;
-  auto bar_kv_full = [&](int s) { return bar0 + 16 + 8 * s; };
-  auto bar_kv_empty = [&](int s) { return bar0 + 16 + 8 * (L::STAGES + s); };
-  const uint32_t barx = bar0 + 16 + 16 * L::STAGES;
-  auto bar_s_full = [&](int i) { return barx + 8 * i; };
-  auto bar_p_full = [&](int i) { return barx + 16 + 8 * i; };
-  auto bar_o_full = [&](int i) { return barx + 32 + 8 * i; };
-  auto bar_o_empty = [&](int i) { return barx + 48 + 8 * i; };
+  // barrier addresses (8 bytes each)
+  const uint32_t bar_q_full = bar0;                          // [2]
+  const uint32_t bar_q_empty = bar0 + 16;                    // [2]
+  const uint32_t bar_kv_full = bar0 + 32;                    // [STAGES]
+  const uint32_t bar_kv_empty = bar0 + 32 + 8 * L::STAGES;   // [STAGES]
+  const uint32_t barx = bar0 + 32 + 16 * L::STAGES;
+  const uint32_t bar_s_full = barx;        // [2]
+  const uint32_t bar_p_full = barx + 16;   // [2]
+  const uint32_t bar_o_full = barx + 32;   // [2]
+  const uint32_t bar_o_empty = barx + 48;  // [2]
   const uint32_t bar_done = barx + 64;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const int G = gridDim.x;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_q_full + 8 * b, 1);
+      mbar_init(bar_q_empty + 8 * b, 1);
+    }
     for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(bar_kv_full(s), 1);
-      mbar_init(bar_kv_empty(s), 1);
+      mbar_init(bar_kv_full + 8 * s, 1);
+      mbar_init(bar_kv_empty + 8 * s, 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_s_full(i), 1);
-      mbar_init(bar_p_full(i), 4);
-      mbar_init(bar_o_full(i), 1);
-      mbar_init(bar_o_empty(i), 4);
+      mbar_init(bar_s_full + 8 * i, 1);
+      mbar_init(bar_p_full + 8 * i, 4);
+      mbar_init(bar_o_full + 8 * i, 1);
+      mbar_init(bar_o_empty + 8 * i, 4);
     }
     mbar_init(bar_done, 1);
     *abort_flag = 0;
@@ -185,32 +188,39 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       int stage = 0;
-      uint32_t phase = 0, qe_phase = 0;
+      uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0, q_issued = 0, q_parity = 0;  // for draining after a timeout
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+      int nu = 0;  // units this CTA has started
+      for (int k = 0; ok && k * G < p.num_units; ++k) {
+        const int w = unit_of(k, blockIdx.x, G);
+        if (w >= p.num_units) continue;
         const Unit u = decode_unit(p, w);
-        const int nmax = max(u.n[0], u.n[1]);
-        if (!(ok = W.wait(bar_q_empty, qe_phase ^ 1))) break;
-        const int nq = (u.n[0] > 0) + (u.n[1] > 0);
-        mbar_arrive_expect_tx(bar_q_full, nq * L::TILE_BYTES);
+        const int nmax = max(u.n0, u.n1);
+        const int qb = nu & 1;
+        const uint32_t qpar = (nu >> 1) & 1;
+        if (!(ok = W.wait(bar_q_empty + 8 * qb, qpar ^ 1))) break;
+        mbar_arrive_expect_tx(bar_q_full + 8 * qb, ((u.n0 > 0) + (u.n1 > 0)) * L::TILE_BYTES);
+#pragma unroll
         for (int i = 0; i < 2; ++i) {
-          if (u.n[i] == 0) continue;
+          if ((i ? u.n1 : u.n0) == 0) continue;
+#pragma unroll
           for (int b = 0; b < L::BOXES; ++b)
-            tma_load_3d(q_smem + i * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64, u.qb * 2 * BM + i * BM,
-                        u.bh, bar_q_full);
+            tma_load_3d(q_smem + (2 * qb + i) * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64,
+                        u.qb * 2 * BM + i * BM, u.bh, bar_q_full + 8 * qb);
         }
-        q_issued = 1;
-        q_parity = qe_phase;
-        qe_phase ^= 1;
+        q_issued |= 1u << qb;
+        q_parity = (q_parity & ~(1u << qb)) | (qpar << qb);
+        ++nu;
         for (int j = 0; ok && j < nmax; ++j) {
+#pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
-            if (!(ok = W.wait(bar_kv_empty(stage), phase ^ 1))) break;
-            mbar_arrive_expect_tx(bar_kv_full(stage), L::TILE_BYTES);
-            const CUtensorMap* tm = kv == 0 ? &tmK : &tmV;
+            if (!(ok = W.wait(bar_kv_empty + 8 * stage, phase ^ 1))) break;
+            mbar_arrive_expect_tx(bar_kv_full + 8 * stage, L::TILE_BYTES);
+#pragma unroll
             for (int b = 0; b < L::BOXES; ++b)
-              tma_load_3d(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, tm, b * 64, j * BN, u.bh,
-                          bar_kv_full(stage));
+              tma_load_3d(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, kv == 0 ? &tmK : &tmV, b * 64, j * BN,
+                          u.bh, bar_kv_full + 8 * stage);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == L::STAGES) {
@@ -221,9 +231,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
       if (!ok) {  // let every copy already issued land before the CTA exits
-        if (q_issued) W.drain(bar_q_full, q_parity);
+        for (int b = 0; b < 2; ++b)
+          if (q_issued & (1u << b)) W.drain(bar_q_full + 8 * b, (q_parity >> b) & 1u);
         for (int s = 0; s < L::STAGES; ++s)
-          if (issued & (1u << s)) W.drain(bar_kv_full(s), (issued_parity >> s) & 1u);
+          if (issued & (1u << s)) W.drain(bar_kv_full + 8 * s, (issued_parity >> s) & 1u);
       }
     }
     __syncwarp();
@@ -232,94 +243,115 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (lane == 0) {
       constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);   // S = Q K^T: both K-major
       constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, D, 1);   // O += P V: V is MN-major
+      // Descriptor halves: the address field (low 14 bits, in 16-byte units) is the
+      // only part that changes, and every offset added below stays inside it.
+      const uint64_t dqk = make_sdesc_sw128(sbase, 16, 1024);        // K-major tiles (Q, K)
+      const uint64_t dvv = make_sdesc_sw128(sbase, BOX_BYTES, 1024); // MN-major tiles (V)
+      const uint32_t dqk_lo = uint32_t(dqk), dqk_hi = uint32_t(dqk >> 32);
+      const uint32_t dv_lo = uint32_t(dvv), dv_hi = uint32_t(dvv >> 32);
       int stage = 0;
-      uint32_t phase = 0, qf_phase = 0;
-      uint32_t pf_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
+      uint32_t phase = 0;
+      uint32_t pf0 = 0, pf1 = 0, oe0 = 0, oe1 = 0;
       bool ok = true;
-      auto take = [&](int& s_out) -> bool {  // the next filled ring slot
-        s_out = stage;
-        if (!W.wait(bar_kv_full(stage), phase)) return false;
-        if (++stage == L::STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-        tc_fence_after();
-        return true;
-      };
-      auto issue_s = [&](int i, int ks) {  // S_i = Q_i K^T over d in steps of 16
-        const uint32_t qa = q_smem + i * L::TILE_BYTES;
-        const uint32_t ka = kv_smem + ks * L::TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * BOX_BYTES + (kk % 4) * 32;
-          mma_ss(tmem + L::s_col(i), make_sdesc_sw128(qa + off, 16, 1024), make_sdesc_sw128(ka + off, 16, 1024),
-                 IDESC_S, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int i, int vs, bool acc) {  // O_i (+)= P_i V over keys in steps of 16
-        const uint32_t va = kv_smem + vs * L::TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + L::o_col(i), tmem + L::s_col(i) + kk * 8, make_sdesc_sw128(va + kk * 2048, BOX_BYTES, 1024),
-                 IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-      };
-      for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+      int nu = 0;
+      for (int k = 0; ok && k * G < p.num_units; ++k) {
+        const int w = unit_of(k, blockIdx.x, G);
+        if (w >= p.num_units) continue;
         const Unit u = decode_unit(p, w);
-        const int n0 = u.n[0], n1 = u.n[1], nmax = max(n0, n1);
+        const int n0 = u.n0, n1 = u.n1, nmax = max(n0, n1);
         const int last_i = n1 > 0 ? 1 : 0;
-        if (!(ok = W.wait(bar_q_full, qf_phase))) break;
-        qf_phase ^= 1;
+        const int qb = nu & 1;
+        if (!(ok = W.wait(bar_q_full + 8 * qb, (nu >> 1) & 1))) break;
+        ++nu;
         tc_fence_after();
-        int ks;
-        if (!(ok = take(ks))) break;
-        for (int i = 0; i < 2; ++i) {
-          if (u.n[i] == 0) continue;
-          issue_s(i, ks);
-          mma_commit(bar_s_full(i));
-          if (i == last_i && u.n[i] == 1) mma_commit(bar_q_empty);
+        const uint32_t q_lo0 = dqk_lo + ((L::Q_OFF + 2 * qb * L::TILE_BYTES) >> 4);
+        // S_i = Q_i K^T over d in steps of 16 (stage ks of the ring)
+#define FA_ISSUE_S(i, ks)                                                                                 \
+  {                                                                                                       \
+    const uint32_t a0 = q_lo0 + (((i) * L::TILE_BYTES) >> 4);                                             \
+    const uint32_t b0 = dqk_lo + ((L::KV_OFF + (ks) * L::TILE_BYTES) >> 4);                               \
+    _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                               \
+      const uint32_t off = (((kk / 4) * BOX_BYTES + (kk % 4) * 32) >> 4);                                 \
+      mma_ss_lohi(tmem + L::s_col(i), a0 + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);     \
+    }                                                                                                     \
+  }
+        // O_i (+)= P_i V over keys in steps of 16 (stage vs of the ring)
+#define FA_ISSUE_PV(i, vs, acc)                                                                           \
+  {                                                                                                       \
+    const uint32_t b0 = dv_lo + ((L::KV_OFF + (vs) * L::TILE_BYTES) >> 4);                                \
+    _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                                \
+      mma_ts_lohi(tmem + L::o_col(i), tmem + L::s_col(i) + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi,        \
+                  IDESC_PV, ((acc) || kk > 0) ? 1u : 0u);                                                 \
+  }
+#define FA_TAKE(slot)                                                  \
+  {                                                                    \
+    slot = stage;                                                      \
+    if (!(ok = W.wait(bar_kv_full + 8 * stage, phase))) break;         \
+    if (++stage == L::STAGES) {                                        \
+      stage = 0;                                                       \
+      phase ^= 1;                                                      \
+    }                                                                  \
+    tc_fence_after();                                                  \
+  }
+        int ks = 0;
+        do {
+          FA_TAKE(ks);
+        } while (0);
+        if (!ok) break;
+        if (n0 > 0) {
+          FA_ISSUE_S(0, ks);
+          mma_commit(bar_s_full);
+          if (last_i == 0 && n0 == 1) mma_commit(bar_q_empty + 8 * qb);
         }
-        mma_commit(bar_kv_empty(ks));
-        for (int j = 0; ok && j < nmax; ++j) {
-          int vs;
-          if (!(ok = take(vs))) break;
-          int ks1 = -1;
+        if (n1 > 0) {
+          FA_ISSUE_S(1, ks);
+          mma_commit(bar_s_full + 8);
+          if (n1 == 1) mma_commit(bar_q_empty + 8 * qb);
+        }
+        mma_commit(bar_kv_empty + 8 * ks);
+        for (int j = 0; j < nmax; ++j) {
+          int vs = 0, ks1 = -1;
+          FA_TAKE(vs);
           if (j < n0) {
             if (j == 0) {
-              if (!(ok = W.wait(bar_o_empty(0), oe_phase[0] ^ 1))) break;
-              oe_phase[0] ^= 1;
+              if (!(ok = W.wait(bar_o_empty, oe0 ^ 1))) break;
+              oe0 ^= 1;
             }
-            if (!(ok = W.wait(bar_p_full(0), pf_phase[0]))) break;
-            pf_phase[0] ^= 1;
+            if (!(ok = W.wait(bar_p_full, pf0))) break;
+            pf0 ^= 1;
             tc_fence_after();
-            issue_pv(0, vs, j > 0);
-            if (j + 1 == n0) mma_commit(bar_o_full(0));
+            FA_ISSUE_PV(0, vs, j > 0);
+            if (j + 1 == n0) mma_commit(bar_o_full);
             if (j + 1 < n0) {
-              if (!(ok = take(ks1))) break;
-              issue_s(0, ks1);
-              mma_commit(bar_s_full(0));
-              if (last_i == 0 && j + 2 == n0) mma_commit(bar_q_empty);
+              FA_TAKE(ks1);
+              FA_ISSUE_S(0, ks1);
+              mma_commit(bar_s_full);
+              if (last_i == 0 && j + 2 == n0) mma_commit(bar_q_empty + 8 * qb);
             }
           }
           if (j < n1) {
             if (j == 0) {
-              if (!(ok = W.wait(bar_o_empty(1), oe_phase[1] ^ 1))) break;
-              oe_phase[1] ^= 1;
+              if (!(ok = W.wait(bar_o_empty + 8, oe1 ^ 1))) break;
+              oe1 ^= 1;
             }
-            if (!(ok = W.wait(bar_p_full(1), pf_phase[1]))) break;
-            pf_phase[1] ^= 1;
+            if (!(ok = W.wait(bar_p_full + 8, pf1))) break;
+            pf1 ^= 1;
             tc_fence_after();
-            issue_pv(1, vs, j > 0);
-            if (j + 1 == n1) mma_commit(bar_o_full(1));
+            FA_ISSUE_PV(1, vs, j > 0);
+            if (j + 1 == n1) mma_commit(bar_o_full + 8);
           }
-          mma_commit(bar_kv_empty(vs));
+          mma_commit(bar_kv_empty + 8 * vs);
           if (j + 1 < n1) {
-            if (ks1 < 0 && !(ok = take(ks1))) break;
-            issue_s(1, ks1);
-            mma_commit(bar_s_full(1));
-            if (j + 2 == n1) mma_commit(bar_q_empty);
+            if (ks1 < 0) FA_TAKE(ks1);
+            FA_ISSUE_S(1, ks1);
+            mma_commit(bar_s_full + 8);
+            if (j + 2 == n1) mma_commit(bar_q_empty + 8 * qb);
           }
-          if (ks1 >= 0) mma_commit(bar_kv_empty(ks1));
+          if (ks1 >= 0) mma_commit(bar_kv_empty + 8 * ks1);
         }
+#undef FA_ISSUE_S
+#undef FA_ISSUE_PV
+#undef FA_TAKE
       }
       // every MMA and every commit arrival has landed before TMEM is freed
       mma_commit(bar_done);
@@ -328,18 +360,22 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    const int i = warp / 4;        // query tile of this warpgroup
-    const int wq = warp % 4;       // TMEM lane quarter this warp may access
+    const int i = warp / 4;         // query tile of this warpgroup
+    const int wq = warp % 4;        // TMEM lane quarter this warp may access
     const int rt = wq * 32 + lane;  // row within the query tile
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_off + L::s_col(i);
     const uint32_t t_o = tmem + lane_off + L::o_col(i);
+    const uint32_t my_s_full = bar_s_full + 8 * i, my_p_full = bar_p_full + 8 * i;
+    const uint32_t my_o_full = bar_o_full + 8 * i, my_o_empty = bar_o_empty + 8 * i;
     const float sl2 = p.scale_log2;
     uint32_t sf_phase = 0, of_phase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < p.num_units; w += gridDim.x) {
+    for (int k = 0; ok && k * G < p.num_units; ++k) {
+      const int w = unit_of(k, blockIdx.x, G);
+      if (w >= p.num_units) continue;
       const Unit u = decode_unit(p, w);
-      const int n = u.n[i];
+      const int n = i ? u.n1 : u.n0;
       if (n == 0) continue;
       const int q0 = u.qb * 2 * BM + i * BM;
       const int row = q0 + rt;
@@ -347,7 +383,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       float l = 0.f;            // sum of the fp32 weights: the softmax denominator of the LSE
       float lr = 0.f;           // sum of the bf16 weights the P V product used: divides O
       for (int j = 0; j < n; ++j) {
-        if (!(ok = W.wait(bar_s_full(i), sf_phase))) break;
+        if (!(ok = W.wait(my_s_full, sf_phase))) break;
         sf_phase ^= 1;
         tc_fence_after();
         uint32_t sr[BN];
@@ -383,22 +419,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           rescale = true;
         }
         const float nm = -m_run;
-        float l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+        float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;  // fp32 weights, two packed chains
+        float lr0 = 0.f, lr1 = 0.f;                         // bf16 weights
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(u2f(sr[32 * c + 2 * e]), sl2, nm));
-            const float p1 = ex2_approx(fmaf(u2f(sr[32 * c + 2 * e + 1]), sl2, nm));
-            l0 += p0;
-            l1 += p1;
+            float x0, x1;
+            ffma2(x0, x1, u2f(sr[32 * c + 2 * e]), u2f(sr[32 * c + 2 * e + 1]), sl2, nm);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            if (e & 1)
+              fadd2(lb0, lb1, p0, p1);
+            else
+              fadd2(la0, la1, p0, p1);
             pk[e] = pack_bf16x2(p0, p1);
             add_bf16x2_f32(pk[e], lr0, lr1);
           }
           tmem_st16(t_s + c * 16, pk);
         }
-        l += l0 + l1;
+        l += (la0 + la1) + (lb0 + lb1);
         lr += lr0 + lr1;
         if (rescale) {  // o *= r; PV_i(j-1) has completed (it was issued before S_i(j))
 #pragma unroll
@@ -413,11 +454,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_p_full(i));
+        if (lane == 0) mbar_arrive(my_p_full);
       }
       if (!ok) break;
-      // epilogue: O = o / l in bf16, LSE = ln(2) (m + log2 l)
-      if (!(ok = W.wait(bar_o_full(i), of_phase))) break;
+      // epilogue: O = o / lr in bf16, LSE = ln(2) (m + log2 l)
+      if (!(ok = W.wait(my_o_full, of_phase))) break;
       of_phase ^= 1;
       tc_fence_after();
       const float inv_l = 1.f / lr;
@@ -438,7 +479,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (row < p.T) p.lse[static_cast<size_t>(u.bh) * p.T + row] = (m_run + log2f(l)) * LN2;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_o_empty(i));
+      if (lane == 0) mbar_arrive(my_o_empty);
     }
   }
 

@@ -187,4 +187,41 @@ __device__ __forceinline__ void add_bf16x2_f32(uint32_t packed, float& acc_lo, f
       : "+f"(acc_lo), "+f"(acc_hi) : "r"(packed));
 }
 
+// (d0, d1) = (a0, a1) * b + c on the packed fp32x2 FMA path.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (acc0, acc1) += (a0, a1) on the packed fp32x2 add path.
+__device__ __forceinline__ void fadd2(float& acc0, float& acc1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rc, {%0, %1};\n\t"
+      "add.rn.f32x2 rc, ra, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(acc0), "+f"(acc1) : "f"(a0), "f"(a1));
+}
+
+// tcgen05.mma with operand descriptors given as 32-bit halves (the high halves
+// never change inside a CTA, so callers keep them fixed and add byte offsets >> 4
+// to the low halves).
+__device__ __forceinline__ void mma_ss_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}"
+      :: "r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void mma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 }  // namespace fa
