@@ -26,6 +26,9 @@
 //   warps 4-7  softmax for query tile 1
 //   warp 8     TMA producer: Q tiles once per unit, then K_j, V_j through a ring
 //   warp 9     TMEM allocator and tcgen05.mma issuer
+// Warps 8 and 9 run their schedules on all 32 lanes (every operand stays
+// warp-uniform); elect.sync inside each TMA, MMA and commit picks the one lane
+// that issues it.
 // A work unit is (batch*head, 256 query rows) = two 128-row query tiles that
 // share every K/V tile loaded.  Tensor Memory (512 columns):
 //   S_0 [0,128)  S_1 [128,256)  O_0 [256,256+d)  O_1 [256+d,256+2d)
@@ -120,6 +123,15 @@ struct Waiter {
   }
 };
 
+// Warp-wide forms for the issuing warps: every lane waits, and the warp agrees on
+// the outcome (a lane that timed out makes the whole warp give up).
+__device__ __forceinline__ bool wait_all(const Waiter& W, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, W.wait(bar, parity));
+}
+__device__ __forceinline__ bool drain_all(const Waiter& W, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, W.drain(bar, parity));
+}
+
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
@@ -182,11 +194,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const Waiter W{abort_flag, p.timeout_ns};
 
   if (warp == PRODUCER_WARP) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
+    // ------------------------------------------------------------ TMA producer (whole warp, one lane issues)
+    {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0, q_issued = 0, q_parity = 0;  // for draining after a timeout
@@ -199,14 +213,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int nmax = max(u.n0, u.n1);
         const int qb = nu & 1;
         const uint32_t qpar = (nu >> 1) & 1;
-        if (!(ok = W.wait(bar_q_empty + 8 * qb, qpar ^ 1))) break;
-        mbar_arrive_expect_tx(bar_q_full + 8 * qb, ((u.n0 > 0) + (u.n1 > 0)) * L::TILE_BYTES);
+        if (!(ok = wait_all(W, bar_q_empty + 8 * qb, qpar ^ 1))) break;
+        mbar_arrive_expect_tx_elect(bar_q_full + 8 * qb, ((u.n0 > 0) + (u.n1 > 0)) * L::TILE_BYTES);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if ((i ? u.n1 : u.n0) == 0) continue;
 #pragma unroll
           for (int b = 0; b < L::BOXES; ++b)
-            tma_load_3d(q_smem + (2 * qb + i) * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64,
+            tma_load_3d_elect(q_smem + (2 * qb + i) * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64,
                         u.qb * 2 * BM + i * BM, u.bh, bar_q_full + 8 * qb);
         }
         q_issued |= 1u << qb;
@@ -215,11 +229,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int j = 0; ok && j < nmax; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
-            if (!(ok = W.wait(bar_kv_empty + 8 * stage, phase ^ 1))) break;
-            mbar_arrive_expect_tx(bar_kv_full + 8 * stage, L::TILE_BYTES);
+            if (!(ok = wait_all(W, bar_kv_empty + 8 * stage, phase ^ 1))) break;
+            mbar_arrive_expect_tx_elect(bar_kv_full + 8 * stage, L::TILE_BYTES);
 #pragma unroll
             for (int b = 0; b < L::BOXES; ++b)
-              tma_load_3d(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, kv == 0 ? &tmK : &tmV, b * 64, j * BN,
+              tma_load_3d_elect(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, kv == 0 ? &tmK : &tmV, b * 64, j * BN,
                           u.bh, bar_kv_full + 8 * stage);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -232,15 +246,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       }
       if (!ok) {  // let every copy already issued land before the CTA exits
         for (int b = 0; b < 2; ++b)
-          if (q_issued & (1u << b)) W.drain(bar_q_full + 8 * b, (q_parity >> b) & 1u);
+          if (q_issued & (1u << b)) drain_all(W, bar_q_full + 8 * b, (q_parity >> b) & 1u);
         for (int s = 0; s < L::STAGES; ++s)
-          if (issued & (1u << s)) W.drain(bar_kv_full + 8 * s, (issued_parity >> s) & 1u);
+          if (issued & (1u << s)) drain_all(W, bar_kv_full + 8 * s, (issued_parity >> s) & 1u);
       }
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp, one lane issues)
+    {
       constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);   // S = Q K^T: both K-major
       constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, D, 1);   // O += P V: V is MN-major
       // Descriptor halves: the address field (low 14 bits, in 16-byte units) is the
@@ -261,7 +275,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int n0 = u.n0, n1 = u.n1, nmax = max(n0, n1);
         const int last_i = n1 > 0 ? 1 : 0;
         const int qb = nu & 1;
-        if (!(ok = W.wait(bar_q_full + 8 * qb, (nu >> 1) & 1))) break;
+        if (!(ok = wait_all(W, bar_q_full + 8 * qb, (nu >> 1) & 1))) break;
         ++nu;
         tc_fence_after();
         const uint32_t q_lo0 = dqk_lo + ((L::Q_OFF + 2 * qb * L::TILE_BYTES) >> 4);
@@ -272,7 +286,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t b0 = dqk_lo + ((L::KV_OFF + (ks) * L::TILE_BYTES) >> 4);                               \
     _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                               \
       const uint32_t off = (((kk / 4) * BOX_BYTES + (kk % 4) * 32) >> 4);                                 \
-      mma_ss_lohi(tmem + L::s_col(i), a0 + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);     \
+      mma_ss_elect(tmem + L::s_col(i), a0 + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);     \
     }                                                                                                     \
   }
         // O_i (+)= P_i V over keys in steps of 16 (stage vs of the ring)
@@ -280,13 +294,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   {                                                                                                       \
     const uint32_t b0 = dv_lo + ((L::KV_OFF + (vs) * L::TILE_BYTES) >> 4);                                \
     _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                                \
-      mma_ts_lohi(tmem + L::o_col(i), tmem + L::s_col(i) + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi,        \
+      mma_ts_elect(tmem + L::o_col(i), tmem + L::s_col(i) + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi,        \
                   IDESC_PV, ((acc) || kk > 0) ? 1u : 0u);                                                 \
   }
 #define FA_TAKE(slot)                                                  \
   {                                                                    \
     slot = stage;                                                      \
-    if (!(ok = W.wait(bar_kv_full + 8 * stage, phase))) break;         \
+    if (!(ok = wait_all(W, bar_kv_full + 8 * stage, phase))) break;         \
     if (++stage == L::STAGES) {                                        \
       stage = 0;                                                       \
       phase ^= 1;                                                      \
@@ -300,62 +314,62 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (!ok) break;
         if (n0 > 0) {
           FA_ISSUE_S(0, ks);
-          mma_commit(bar_s_full);
-          if (last_i == 0 && n0 == 1) mma_commit(bar_q_empty + 8 * qb);
+          mma_commit_elect(bar_s_full);
+          if (last_i == 0 && n0 == 1) mma_commit_elect(bar_q_empty + 8 * qb);
         }
         if (n1 > 0) {
           FA_ISSUE_S(1, ks);
-          mma_commit(bar_s_full + 8);
-          if (n1 == 1) mma_commit(bar_q_empty + 8 * qb);
+          mma_commit_elect(bar_s_full + 8);
+          if (n1 == 1) mma_commit_elect(bar_q_empty + 8 * qb);
         }
-        mma_commit(bar_kv_empty + 8 * ks);
+        mma_commit_elect(bar_kv_empty + 8 * ks);
         for (int j = 0; j < nmax; ++j) {
           int vs = 0, ks1 = -1;
           FA_TAKE(vs);
           if (j < n0) {
             if (j == 0) {
-              if (!(ok = W.wait(bar_o_empty, oe0 ^ 1))) break;
+              if (!(ok = wait_all(W, bar_o_empty, oe0 ^ 1))) break;
               oe0 ^= 1;
             }
-            if (!(ok = W.wait(bar_p_full, pf0))) break;
+            if (!(ok = wait_all(W, bar_p_full, pf0))) break;
             pf0 ^= 1;
             tc_fence_after();
             FA_ISSUE_PV(0, vs, j > 0);
-            if (j + 1 == n0) mma_commit(bar_o_full);
+            if (j + 1 == n0) mma_commit_elect(bar_o_full);
             if (j + 1 < n0) {
               FA_TAKE(ks1);
               FA_ISSUE_S(0, ks1);
-              mma_commit(bar_s_full);
-              if (last_i == 0 && j + 2 == n0) mma_commit(bar_q_empty + 8 * qb);
+              mma_commit_elect(bar_s_full);
+              if (last_i == 0 && j + 2 == n0) mma_commit_elect(bar_q_empty + 8 * qb);
             }
           }
           if (j < n1) {
             if (j == 0) {
-              if (!(ok = W.wait(bar_o_empty + 8, oe1 ^ 1))) break;
+              if (!(ok = wait_all(W, bar_o_empty + 8, oe1 ^ 1))) break;
               oe1 ^= 1;
             }
-            if (!(ok = W.wait(bar_p_full + 8, pf1))) break;
+            if (!(ok = wait_all(W, bar_p_full + 8, pf1))) break;
             pf1 ^= 1;
             tc_fence_after();
             FA_ISSUE_PV(1, vs, j > 0);
-            if (j + 1 == n1) mma_commit(bar_o_full + 8);
+            if (j + 1 == n1) mma_commit_elect(bar_o_full + 8);
           }
-          mma_commit(bar_kv_empty + 8 * vs);
+          mma_commit_elect(bar_kv_empty + 8 * vs);
           if (j + 1 < n1) {
             if (ks1 < 0) FA_TAKE(ks1);
             FA_ISSUE_S(1, ks1);
-            mma_commit(bar_s_full + 8);
-            if (j + 2 == n1) mma_commit(bar_q_empty + 8 * qb);
+            mma_commit_elect(bar_s_full + 8);
+            if (j + 2 == n1) mma_commit_elect(bar_q_empty + 8 * qb);
           }
-          if (ks1 >= 0) mma_commit(bar_kv_empty + 8 * ks1);
+          if (ks1 >= 0) mma_commit_elect(bar_kv_empty + 8 * ks1);
         }
 #undef FA_ISSUE_S
 #undef FA_ISSUE_PV
 #undef FA_TAKE
       }
       // every MMA and every commit arrival has landed before TMEM is freed
-      mma_commit(bar_done);
-      W.drain(bar_done, 0);
+      mma_commit_elect(bar_done);
+      drain_all(W, bar_done, 0);
     }
     __syncwarp();
   } else {
