@@ -8,7 +8,7 @@ the library has not been built, importing works but the first call raises.
 
 Entry points (same names as the C ABI):
     fa_fwd(q, k, v, o, lse, causal, scale, stream=None)
-    fa_status_string(code), fa_device_status(stream=None)
+    fa_status_string(code), fa_device_status(stream=None), fa_selftest_wait_timeout(us, stream=None)
     fa_fwd_launch_shape(B, H, T, d, causal, num_sms), fa_version()
 and the convenience wrapper ``attention(q, k, v, causal, scale=None)`` that
 allocates O and LSE with PyTorch.
@@ -22,7 +22,8 @@ import os
 from ._build import build, lib_path  # noqa: F401
 
 __all__ = [
-    "FAError", "fa_fwd", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_version",
+    "FAError", "fa_fwd", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout",
+    "fa_version",
     "attention", "load_library", "STATUS",
 ]
 
@@ -32,7 +33,8 @@ STATUS = {
     7: "FA_ERR_LAUNCH", 8: "FA_ERR_DEVICE_TIMEOUT", 9: "FA_ERR_BAD_ARG", 10: "FA_ERR_BAD_POINTER",
     11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA",
 }
-EXPORTED = ["fa_fwd", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_version"]
+EXPORTED = ["fa_fwd", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout",
+            "fa_version"]
 
 
 class FAError(RuntimeError):
@@ -65,6 +67,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_device_status.restype = i
     lib.fa_fwd_launch_shape.argtypes = [i, i, i, i, i, i] + [ctypes.POINTER(i)] * 3
     lib.fa_fwd_launch_shape.restype = i
+    lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+    lib.fa_selftest_wait_timeout.restype = i
     lib.fa_version.argtypes = []
     lib.fa_version.restype = ctypes.c_char_p
     if path == lib_path():
@@ -107,6 +111,13 @@ def fa_device_status(stream=None) -> int:
     if code:
         raise FAError(code, "fa_device_status")
     return out.value
+
+
+def fa_selftest_wait_timeout(timeout_us: int, stream=None) -> None:
+    """Enqueues the bounded-wait self-test kernel (see include/fa.h); read the outcome with fa_device_status."""
+    code = load_library().fa_selftest_wait_timeout(int(timeout_us), ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_selftest_wait_timeout")
 
 
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:

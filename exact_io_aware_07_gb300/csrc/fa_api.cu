@@ -16,11 +16,11 @@ namespace {
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-using PointerAttrFn = CUresult (*)(void*, CUpointer_attribute, CUdeviceptr);
+using PointerAttrsFn = CUresult (*)(unsigned int, CUpointer_attribute*, void**, CUdeviceptr);
 
 struct DriverFns {
   EncodeTiledFn encode_tiled = nullptr;
-  PointerAttrFn pointer_attr = nullptr;
+  PointerAttrsFn pointer_attrs = nullptr;
 };
 
 // Driver entry points, resolved through the runtime so the library needs no link to libcuda.
@@ -35,10 +35,10 @@ const DriverFns& driver_fns() {
         q == cudaDriverEntryPointSuccess)
       fns.encode_tiled = reinterpret_cast<EncodeTiledFn>(f);
     f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 4000, cudaEnableDefault, &q) ==
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttributes", &f, 7000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fns.pointer_attr = reinterpret_cast<PointerAttrFn>(f);
+      fns.pointer_attrs = reinterpret_cast<PointerAttrsFn>(f);
   });
   return fns;
 }
@@ -88,23 +88,22 @@ fa_status current_device(int* dev_out, int* num_sms) {
   return FA_OK;
 }
 
-// `p` must be device memory of device `dev`, and [p, p + bytes) must lie in one allocation.
+// `p` must be device memory of device `dev`, and [p, p + bytes) must lie in one
+// allocation.  One driver query per pointer (memory type, ordinal, range).
 fa_status check_device_range(const void* p, size_t bytes, int dev) {
   const DriverFns& fns = driver_fns();
-  if (!fns.pointer_attr) return FA_ERR_CUDA;
+  if (!fns.pointer_attrs) return FA_ERR_CUDA;
   const CUdeviceptr dp = reinterpret_cast<CUdeviceptr>(p);
   unsigned int mem_type = 0;
   int ordinal = -1;
   CUdeviceptr base = 0;
   size_t size = 0;
-  if (fns.pointer_attr(&mem_type, CU_POINTER_ATTRIBUTE_MEMORY_TYPE, dp) != CUDA_SUCCESS ||
-      mem_type != CU_MEMORYTYPE_DEVICE)
-    return FA_ERR_BAD_POINTER;
-  if (fns.pointer_attr(&ordinal, CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL, dp) != CUDA_SUCCESS || ordinal != dev)
-    return FA_ERR_BAD_POINTER;
-  if (fns.pointer_attr(&base, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS ||
-      fns.pointer_attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS)
-    return FA_ERR_BAD_POINTER;
+  CUpointer_attribute attrs[4] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL,
+                                  CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, CU_POINTER_ATTRIBUTE_RANGE_SIZE};
+  void* data[4] = {&mem_type, &ordinal, &base, &size};
+  // an address the driver does not know leaves the values untouched (type 0) or fails
+  if (fns.pointer_attrs(4, attrs, data, dp) != CUDA_SUCCESS) return FA_ERR_BAD_POINTER;
+  if (mem_type != CU_MEMORYTYPE_DEVICE || ordinal != dev || size == 0) return FA_ERR_BAD_POINTER;
   if (dp < base || dp - base > size || bytes > size - (dp - base)) return FA_ERR_BAD_POINTER;
   return FA_OK;
 }
@@ -131,7 +130,7 @@ fa_status validate_host(const void* q, const void* k, const void* v, const void*
   return FA_OK;
 }
 
-bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
+bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
   const DriverFns& fns = driver_fns();
   if (!fns.encode_tiled) return false;
   // 3-D view (d, T, B*H): a box never crosses from one head into the next, and
@@ -143,6 +142,34 @@ bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
   return fns.encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                           elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Encoded descriptors, reused when the same tensor comes back (encoding reads no
+// memory, so a cached descriptor is exactly what encoding again would give).
+struct MapCacheEntry {
+  const void* base = nullptr;
+  int BH = 0, T = 0, d = 0;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 16;
+MapCacheEntry g_map_cache[kMapCache];
+std::mutex g_map_mu;
+
+bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
+  const size_t slot = (reinterpret_cast<uintptr_t>(base) >> 8) % kMapCache;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapCacheEntry& e = g_map_cache[slot];
+  if (e.base == base && e.BH == BH && e.T == T && e.d == d) {
+    *map = e.map;
+    return true;
+  }
+  if (!encode_tensor_map(map, base, BH, T, d)) return false;
+  e.base = base;
+  e.BH = BH;
+  e.T = T;
+  e.d = d;
+  e.map = *map;
+  return true;
 }
 
 }  // namespace
@@ -232,6 +259,18 @@ fa_status fa_fwd_launch_shape(int B, int H, int T, int d, int causal, int num_sm
   *grid = static_cast<int>(units < num_sms ? units : num_sms);
   *threads = fa::fa_fwd_threads();
   *smem_bytes = fa::fa_fwd_smem_bytes(d);
+  return FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream) {
+  if (timeout_us < 1 || timeout_us > 2000000) return FA_ERR_BAD_ARG;
+  int dev = 0, num_sms = 0;
+  fa_status st = current_device(&dev, &num_sms);
+  if (st != FA_OK) return st;
+  if (fa::launch_wait_selftest(static_cast<unsigned long long>(timeout_us) * 1000ull, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
   return FA_OK;
 }
 

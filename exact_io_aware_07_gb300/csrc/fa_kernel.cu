@@ -19,7 +19,13 @@
 // multiplies by, and O = sum p~ v / lr is a convex combination of the value
 // rows under exactly the weights used (a row dominated by one key returns that
 // key's value row unchanged, whatever the stale m); l sums the fp32 weights and
-// gives the LSE without the bf16 rounding of the weights.
+// gives the LSE without the bf16 rounding of the weights.  At d = 64 the tensor
+// core forms lr: each V tile is extended, inside the MMA operand, by 16 columns
+// of ones (a constant shared-memory block reached through the descriptor's
+// leading-byte offset), so O's column 64 accumulates sum p~ with the same
+// arithmetic as the numerator, at no MMA cost (N = 80 runs as fast as N = 64).
+// At d = 128 Tensor Memory has no room for the extra columns and the softmax
+// threads sum the packed weights.
 //
 // Roles (320 threads, one CTA per SM, persistent over work units):
 //   warps 0-3  softmax for query tile 0 of the unit (one TMEM lane = one row per thread)
@@ -61,13 +67,16 @@ struct Layout {
   static constexpr int STAGES = (D == 128) ? 3 : 6;   // K/V ring depth (tiles)
   static constexpr int Q_OFF = 0;                      // 2 units x 2 query tiles (double-buffered)
   static constexpr int KV_OFF = 4 * TILE_BYTES;
-  static constexpr int BAR_OFF = KV_OFF + STAGES * TILE_BYTES;
+  static constexpr bool LR_IN_TMEM = (D == 64);          // the P V MMA also forms sum p~ (see above)
+  static constexpr int ON = LR_IN_TMEM ? D + 16 : D;     // O columns per query tile in TMEM
+  static constexpr int ONES_OFF = KV_OFF + STAGES * TILE_BYTES;   // 128 x 64 bf16 ones (d = 64 only)
+  static constexpr int BAR_OFF = ONES_OFF + (LR_IN_TMEM ? BOX_BYTES : 0);
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2], done
   static constexpr int NUM_BARS = 4 + 2 * STAGES + 8 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // TMEM base slot, abort flag
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
   static __device__ __forceinline__ constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
-  static __device__ __forceinline__ constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * D; }
+  static __device__ __forceinline__ constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * ON; }
 };
 
 struct Unit {
@@ -183,6 +192,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (L::LR_IN_TMEM) {  // the ones block read by the P V MMA (bf16 1.0 everywhere, so swizzle is moot)
+    uint4* ones = reinterpret_cast<uint4*>(smem + L::ONES_OFF);
+    for (int x = threadIdx.x; x < BOX_BYTES / 16; x += NUM_THREADS)
+      ones[x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
   if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
@@ -256,11 +271,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // ------------------------------------------------------------ MMA issuer (whole warp, one lane issues)
     {
       constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);   // S = Q K^T: both K-major
-      constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, D, 1);   // O += P V: V is MN-major
+      constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, L::ON, 1);  // O += P V: V is MN-major
       // Descriptor halves: the address field (low 14 bits, in 16-byte units) is the
       // only part that changes, and every offset added below stays inside it.
       const uint64_t dqk = make_sdesc_sw128(sbase, 16, 1024);        // K-major tiles (Q, K)
-      const uint64_t dvv = make_sdesc_sw128(sbase, BOX_BYTES, 1024); // MN-major tiles (V)
+      // MN-major V tiles; at d = 64 the leading-byte offset of stage 0 reaches the ones block
+      const uint64_t dvv = make_sdesc_sw128(sbase, L::LR_IN_TMEM ? L::ONES_OFF - L::KV_OFF : BOX_BYTES, 1024);
       const uint32_t dqk_lo = uint32_t(dqk), dqk_hi = uint32_t(dqk >> 32);
       const uint32_t dv_lo = uint32_t(dvv), dv_hi = uint32_t(dvv >> 32);
       int stage = 0;
@@ -292,7 +308,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // O_i (+)= P_i V over keys in steps of 16 (stage vs of the ring)
 #define FA_ISSUE_PV(i, vs, acc)                                                                           \
   {                                                                                                       \
-    const uint32_t b0 = dv_lo + ((L::KV_OFF + (vs) * L::TILE_BYTES) >> 4);                                \
+    const uint32_t s16 = ((vs) * L::TILE_BYTES) >> 4;                                                     \
+    const uint32_t b0 = dv_lo + (L::KV_OFF >> 4) + s16 - (L::LR_IN_TMEM ? (s16 << 16) : 0u);            \
     _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                                \
       mma_ts_elect(tmem + L::o_col(i), tmem + L::s_col(i) + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi,        \
                   IDESC_PV, ((acc) || kk > 0) ? 1u : 0u);                                                 \
@@ -410,14 +427,18 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           for (int c = 0; c < BN; ++c)
             if (c >= lim) sr[c] = f2u(-INFINITY);
         }
-        float m4[4];  // four independent max chains over columns 0-7, then 8 columns per step
+        float m8[8];  // eight independent chains of 2-input max (full rate; 3-input max is half rate)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) m4[e] = fmaxf(u2f(sr[2 * e]), u2f(sr[2 * e + 1]));
+        for (int e = 0; e < 8; ++e) m8[e] = u2f(sr[e]);
 #pragma unroll
         for (int c = 8; c < BN; c += 8)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) m4[e] = max3f(m4[e], u2f(sr[c + 2 * e]), u2f(sr[c + 2 * e + 1]));
-        float mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+          for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], u2f(sr[c + e]));
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) m8[e] = fmaxf(m8[e], m8[e + w]);
+        float mx = m8[0];
         mx *= sl2;
         // lazy rescale decision (warp-uniform: TMEM access below is warp-collective)
         float r = 1.f;
@@ -449,7 +470,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             else
               fadd2(la0, la1, p0, p1);
             pk[e] = pack_bf16x2(p0, p1);
-            add_bf16x2_f32(pk[e], lr0, lr1);
+            if (!L::LR_IN_TMEM) add_bf16x2_f32(pk[e], lr0, lr1);
           }
           tmem_st16(t_s + c * 16, pk);
         }
@@ -464,6 +485,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (int e = 0; e < 32; ++e) ov[e] = f2u(u2f(ov[e]) * r);
             tmem_st32(t_o + c * 32, ov);
           }
+          if (L::LR_IN_TMEM) tmem_st1(t_o + D, f2u(u2f(tmem_ld1_wait(t_o + D)) * r));
         }
         tmem_wait_st();
         tc_fence_before();
@@ -475,6 +497,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (!(ok = W.wait(my_o_full, of_phase))) break;
       of_phase ^= 1;
       tc_fence_after();
+      if (L::LR_IN_TMEM) lr = u2f(tmem_ld1_wait(t_o + D));  // sum p~ formed by the P V MMA
       const float inv_l = 1.f / lr;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(u.bh) * p.T + row) * D;
 #pragma unroll
@@ -505,6 +528,22 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// ever arrives on, so the wait runs out after `timeout_ns` and records the
+// timeout in the status word, exactly as a stalled attention launch would.
+__global__ void fa_wait_selftest_kernel(unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const Waiter W{&abort_flag, timeout_ns};
+  if (threadIdx.x == 0) W.wait(smem_u32(&bar), 0);
+}
+
 // ---------------------------------------------------------------- host side
 
 template <int D>
@@ -531,6 +570,11 @@ cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, con
                           const Params& p, int grid, cudaStream_t stream) {
   if (d == 64) return launch<64>(q, k, v, p, grid, stream);
   return launch<128>(q, k, v, p, grid, stream);
+}
+
+cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t stream) {
+  fa_wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns);
+  return cudaGetLastError();
 }
 
 int fa_fwd_smem_bytes(int d) { return d == 64 ? Layout<64>::SMEM_BYTES : Layout<128>::SMEM_BYTES; }

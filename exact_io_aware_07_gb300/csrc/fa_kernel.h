@@ -25,5 +25,6 @@ int fa_fwd_smem_bytes(int d);
 int fa_fwd_threads();
 int fa_fwd_rows_per_unit();
 cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* out);
+cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t stream);
 
 }  // namespace fa

@@ -54,7 +54,7 @@ typedef enum {
   FA_ERR_NO_DEVICE_SUPPORT = 6,     /* the current device is not sm_103 */
   FA_ERR_LAUNCH = 7,                /* the CUDA runtime refused the launch */
   FA_ERR_DEVICE_TIMEOUT = 8,        /* a bounded in-kernel wait ran out */
-  FA_ERR_BAD_ARG = 9,               /* causal is not 0 or 1 */
+  FA_ERR_BAD_ARG = 9,               /* an argument is out of range (causal not 0 or 1, a self-test timeout) */
   FA_ERR_BAD_POINTER = 10,          /* a pointer is not device memory, or its allocation is too small */
   FA_ERR_ALIAS = 11,                /* O or LSE overlaps an input or each other */
   FA_ERR_CUDA = 12                  /* a CUDA runtime or driver query failed */
@@ -92,6 +92,18 @@ fa_status fa_device_status(cudaStream_t stream, int* out);
  */
 fa_status fa_fwd_launch_shape(int B, int H, int T, int d, int causal, int num_sms,
                               int* grid, int* threads, int* smem_bytes);
+
+/*
+ * Self-test of the in-kernel wait bound (no attention involved): enqueues a
+ * one-block kernel whose single waiting thread waits on a barrier that nothing
+ * ever completes, so the wait runs out after `timeout_us` microseconds
+ * (1 .. 2,000,000) and the kernel returns, recording FA_ERR_DEVICE_TIMEOUT in
+ * the device status word that fa_device_status() reads.  Nothing faults or
+ * hangs; the context stays usable.  Returns FA_ERR_BAD_ARG for an
+ * out-of-range timeout, FA_ERR_NO_DEVICE_SUPPORT off sm_103, FA_ERR_LAUNCH if
+ * the launch is refused.
+ */
+fa_status fa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
 
 /* Library version, e.g. "0.1.0". */
 const char* fa_version(void);

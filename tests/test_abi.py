@@ -91,3 +91,8 @@ def test_launch_shape(lib):
     assert g == 1 and s <= 232_448
     with pytest.raises(fa.FAError):
         fa.fa_fwd_launch_shape(1, 1, 128, 80, False, 152)
+
+
+def test_selftest_rejects_bad_timeout(lib):
+    assert lib.fa_selftest_wait_timeout(0, None) == 9
+    assert lib.fa_selftest_wait_timeout(2_000_001, None) == 9
