@@ -64,9 +64,12 @@ template <int D>
 struct Layout {
   static constexpr int TILE_BYTES = BM * D * 2;
   static constexpr int BOXES = D / 64;
-  static constexpr int STAGES = (D == 128) ? 3 : 6;   // K/V ring depth (tiles)
-  static constexpr int Q_OFF = 0;                      // 2 units x 2 query tiles (double-buffered)
-  static constexpr int KV_OFF = 4 * TILE_BYTES;
+  // d = 64: two units' Q tiles resident (the next unit's load overlaps the current
+  // unit); d = 128: one unit's Q tiles, the next unit's prefetched into L2.
+  static constexpr int QBUF = (D == 128) ? 1 : 2;
+  static constexpr int STAGES = (D == 128) ? 4 : 6;   // K/V ring depth (tiles)
+  static constexpr int Q_OFF = 0;                      // [QBUF units][2 query tiles]
+  static constexpr int KV_OFF = QBUF * 2 * TILE_BYTES;
   static constexpr bool LR_IN_TMEM = (D == 64);          // the P V MMA also forms sum p~ (see above)
   static constexpr int ON = LR_IN_TMEM ? D + 16 : D;     // O columns per query tile in TMEM
   static constexpr int ONES_OFF = KV_OFF + STAGES * TILE_BYTES;   // 128 x 64 bf16 ones (d = 64 only)
@@ -78,6 +81,10 @@ struct Layout {
   static __device__ __forceinline__ constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
   static __device__ __forceinline__ constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * ON; }
 };
+
+constexpr int MAX_SMEM_PER_CTA = 232448;  // 227 KB opt-in dynamic shared memory per block on sm_103
+static_assert(Layout<64>::SMEM_BYTES <= MAX_SMEM_PER_CTA && Layout<128>::SMEM_BYTES <= MAX_SMEM_PER_CTA,
+              "shared-memory layout exceeds the per-CTA limit");
 
 struct Unit {
   int bh, qb;
@@ -226,8 +233,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (w >= p.num_units) continue;
         const Unit u = decode_unit(p, w);
         const int nmax = max(u.n0, u.n1);
-        const int qb = nu & 1;
-        const uint32_t qpar = (nu >> 1) & 1;
+        const int qb = nu % L::QBUF;
+        const uint32_t qpar = (nu / L::QBUF) & 1;
         if (!(ok = wait_all(W, bar_q_empty + 8 * qb, qpar ^ 1))) break;
         mbar_arrive_expect_tx_elect(bar_q_full + 8 * qb, ((u.n0 > 0) + (u.n1 > 0)) * L::TILE_BYTES);
 #pragma unroll
@@ -241,6 +248,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         q_issued |= 1u << qb;
         q_parity = (q_parity & ~(1u << qb)) | (qpar << qb);
         ++nu;
+        if (L::QBUF == 1) {  // warm L2 with the next unit's query tiles
+          int k2 = k + 1, w2 = unit_of(k2, blockIdx.x, G);
+          if (w2 >= p.num_units && (k2 + 1) * G < p.num_units) w2 = unit_of(++k2, blockIdx.x, G);
+          if (w2 < p.num_units) {
+            const Unit u2 = decode_unit(p, w2);
+            for (int i = 0; i < 2; ++i)
+              if ((i ? u2.n1 : u2.n0) > 0)
+                for (int b = 0; b < L::BOXES; ++b)
+                  tma_prefetch_l2_3d_elect(&tmQ, b * 64, u2.qb * 2 * BM + i * BM, u2.bh);
+          }
+        }
         for (int j = 0; ok && j < nmax; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
@@ -290,8 +308,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const Unit u = decode_unit(p, w);
         const int n0 = u.n0, n1 = u.n1, nmax = max(n0, n1);
         const int last_i = n1 > 0 ? 1 : 0;
-        const int qb = nu & 1;
-        if (!(ok = wait_all(W, bar_q_full + 8 * qb, (nu >> 1) & 1))) break;
+        const int qb = nu % L::QBUF;
+        if (!(ok = wait_all(W, bar_q_full + 8 * qb, (nu / L::QBUF) & 1))) break;
         ++nu;
         tc_fence_after();
         const uint32_t q_lo0 = dqk_lo + ((L::Q_OFF + 2 * qb * L::TILE_BYTES) >> 4);
