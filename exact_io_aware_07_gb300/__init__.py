@@ -8,10 +8,13 @@ the library has not been built, importing works but the first call raises.
 
 Entry points (same names as the C ABI):
     fa_fwd(q, k, v, o, lse, causal, scale, stream=None)
+    fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, workspace, stream=None)
+    fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits)
     fa_status_string(code), fa_device_status(stream=None), fa_selftest_wait_timeout(us, stream=None)
     fa_fwd_launch_shape(B, H, T, d, causal, num_sms), fa_version()
-and the convenience wrapper ``attention(q, k, v, causal, scale=None)`` that
-allocates O and LSE with PyTorch.
+and the convenience wrappers ``attention(q, k, v, causal, scale=None)`` and
+``attention_splitkv(q, k, v, causal, num_splits, scale=None)`` that allocate O,
+LSE (and the split workspace) with PyTorch.
 """
 from __future__ import annotations
 
@@ -22,19 +25,20 @@ import os
 from ._build import build, lib_path  # noqa: F401
 
 __all__ = [
-    "FAError", "fa_fwd", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout",
-    "fa_version",
-    "attention", "load_library", "STATUS",
+    "FAError", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_status_string", "fa_device_status",
+    "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version",
+    "attention", "attention_splitkv", "load_library", "STATUS", "FA_MAX_SPLITS",
 ]
 
 STATUS = {
     0: "FA_OK", 1: "FA_ERR_NULL_PTR", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_BAD_SHAPE",
     4: "FA_ERR_UNSUPPORTED_HEAD_DIM", 5: "FA_ERR_BAD_SCALE", 6: "FA_ERR_NO_DEVICE_SUPPORT",
     7: "FA_ERR_LAUNCH", 8: "FA_ERR_DEVICE_TIMEOUT", 9: "FA_ERR_BAD_ARG", 10: "FA_ERR_BAD_POINTER",
-    11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA",
+    11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA", 13: "FA_ERR_WORKSPACE",
 }
-EXPORTED = ["fa_fwd", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout",
-            "fa_version"]
+FA_MAX_SPLITS = 256
+EXPORTED = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_status_string", "fa_device_status",
+            "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version"]
 
 
 class FAError(RuntimeError):
@@ -67,6 +71,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_device_status.restype = i
     lib.fa_fwd_launch_shape.argtypes = [i, i, i, i, i, i] + [ctypes.POINTER(i)] * 3
     lib.fa_fwd_launch_shape.restype = i
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_version.argtypes = []
@@ -153,4 +161,50 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=
     o = torch.empty_like(q)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def fa_fwd_splitkv_workspace_bytes(B: int, H: int, T: int, d: int, num_splits: int) -> int:
+    """Bytes of scratch ``fa_fwd_splitkv`` needs (0 for invalid sizes)."""
+    return int(load_library().fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits))
+
+
+def _check_qkv_o_lse(q, k, v, o, lse):
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 (B, H, T, d) tensor")
+    if not (q.shape == k.shape == v.shape == o.shape):
+        raise ValueError("q, k, v and o must have the same shape")
+    B, H, T, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 (B, H, T) tensor")
+    return B, H, T, d
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, causal: bool, scale: float, num_splits: int, workspace, stream=None) -> None:
+    """Split-KV attention into caller-owned tensors; ``workspace`` is a CUDA tensor used as scratch."""
+    B, H, T, d = _check_qkv_o_lse(q, k, v, o, lse)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    code = load_library().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                         B, H, T, d, int(bool(causal)), float(scale), int(num_splits),
+                                         workspace.data_ptr(), nbytes, ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_fwd_splitkv")
+
+
+def attention_splitkv(q, k, v, causal: bool = False, num_splits: int = 2, scale: float | None = None, stream=None):
+    """Allocates O, LSE and the split workspace and runs ``fa_fwd_splitkv``."""
+    import torch
+
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    ws = torch.empty(fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits), dtype=torch.uint8, device=q.device)
+    fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, ws, stream)
     return o, lse

@@ -172,34 +172,32 @@ bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
   return true;
 }
 
-}  // namespace
+struct Prepared {
+  fa::Params p{};
+  CUtensorMap tq, tk, tv;
+  int dev = 0, num_sms = 0;
+};
 
-extern "C" {
-
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int d,
-                 int causal, float scale, cudaStream_t stream) {
+// Validation shared by the entry points, then the TMA descriptors and the
+// launch parameters of a plain (unsplit) launch.
+fa_status prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int d,
+                  int causal, float scale, Prepared* pr) {
   fa_status st = validate_host(q, k, v, o, lse, B, H, T, d, causal, scale);
   if (st != FA_OK) return st;
-  int dev = 0, num_sms = 0;
-  if ((st = current_device(&dev, &num_sms)) != FA_OK) return st;
-
+  if ((st = current_device(&pr->dev, &pr->num_sms)) != FA_OK) return st;
   const int BH = B * H;
-  const size_t n_elem = static_cast<size_t>(BH) * T * d;
-  const size_t qkv_bytes = n_elem * 2;
+  const size_t qkv_bytes = static_cast<size_t>(BH) * T * d * 2;
   const size_t lse_bytes = static_cast<size_t>(BH) * T * 4;
-  for (const void* p : {q, k, v, static_cast<const void*>(o)})
-    if ((st = check_device_range(p, qkv_bytes, dev)) != FA_OK) return st;
-  if ((st = check_device_range(lse, lse_bytes, dev)) != FA_OK) return st;
+  for (const void* x : {q, k, v, static_cast<const void*>(o)})
+    if ((st = check_device_range(x, qkv_bytes, pr->dev)) != FA_OK) return st;
+  if ((st = check_device_range(lse, lse_bytes, pr->dev)) != FA_OK) return st;
   for (const void* in : {q, k, v})
     if (overlaps(o, qkv_bytes, in, qkv_bytes) || overlaps(lse, lse_bytes, in, qkv_bytes)) return FA_ERR_ALIAS;
   if (overlaps(o, qkv_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
-
-  CUtensorMap tq, tk, tv;
-  if (!make_tensor_map(&tq, q, BH, T, d) || !make_tensor_map(&tk, k, BH, T, d) ||
-      !make_tensor_map(&tv, v, BH, T, d))
+  if (!make_tensor_map(&pr->tq, q, BH, T, d) || !make_tensor_map(&pr->tk, k, BH, T, d) ||
+      !make_tensor_map(&pr->tv, v, BH, T, d))
     return FA_ERR_CUDA;
-
-  fa::Params p{};
+  fa::Params& p = pr->p;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.BH = BH;
@@ -210,12 +208,73 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.num_units = BH * p.nqb;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.timeout_ns = kWaitLimitNs;
-  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-  if (fa::launch_fa_fwd(d, tq, tk, tv, p, grid, stream) != cudaSuccess) {
+  p.num_splits = 1;
+  p.split_tiles = p.nk;
+  p.opart = nullptr;
+  p.lsepart = nullptr;
+  return FA_OK;
+}
+
+// Split-KV launch: partials into `ws` ([splits][rows][d] outputs, then [splits][rows] LSE), then the merge.
+fa_status launch_splitkv(Prepared& pr, int d, int num_splits, float* ws, cudaStream_t stream) {
+  fa::Params& p = pr.p;
+  p.split_tiles = (p.nk + num_splits - 1) / num_splits;
+  p.num_splits = (p.nk + p.split_tiles - 1) / p.split_tiles;  // every split holds at least one key tile
+  const size_t rows = static_cast<size_t>(p.BH) * p.T;
+  p.opart = ws;
+  p.lsepart = ws + static_cast<size_t>(p.num_splits) * rows * d;
+  const long long units = static_cast<long long>(p.BH) * p.nqb * p.num_splits;
+  if (units > INT_MAX) return FA_ERR_BAD_SHAPE;
+  p.num_units = static_cast<int>(units);
+  const int grid = p.num_units < pr.num_sms ? p.num_units : pr.num_sms;
+  if (fa::launch_fa_fwd_partial(d, pr.tq, pr.tk, pr.tv, p, grid, stream) != cudaSuccess ||
+      fa::launch_split_combine(d, p, pr.num_sms, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int d,
+                 int causal, float scale, cudaStream_t stream) {
+  Prepared pr;
+  fa_status st = prepare(q, k, v, o, lse, B, H, T, d, causal, scale, &pr);
+  if (st != FA_OK) return st;
+  const int grid = pr.p.num_units < pr.num_sms ? pr.p.num_units : pr.num_sms;
+  if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, pr.p, grid, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int T, int d, int num_splits) {
+  if (B < 1 || H < 1 || T < 1 || (d != 64 && d != 128) || num_splits < 1 || num_splits > FA_MAX_SPLITS) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * T;
+  const size_t bytes = static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 1) * 4;
+  return (bytes + 255) / 256 * 256;
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T,
+                         int d, int causal, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_BAD_ARG;
+  Prepared pr;
+  fa_status st = prepare(q, k, v, o, lse, B, H, T, d, causal, scale, &pr);
+  if (st != FA_OK) return st;
+  const size_t need = fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return FA_ERR_MISALIGNED;
+  if ((st = check_device_range(workspace, need, pr.dev)) != FA_OK) return st;
+  const size_t qkv_bytes = static_cast<size_t>(B) * H * T * d * 2, lse_bytes = static_cast<size_t>(B) * H * T * 4;
+  for (const void* x : {q, k, v, static_cast<const void*>(o)})
+    if (overlaps(workspace, need, x, qkv_bytes)) return FA_ERR_ALIAS;
+  if (overlaps(workspace, need, lse, lse_bytes)) return FA_ERR_ALIAS;
+  return launch_splitkv(pr, d, num_splits, static_cast<float*>(workspace), stream);
 }
 
 const char* fa_status_string(fa_status s) {
@@ -233,6 +292,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_BAD_POINTER: return "a pointer is not device memory of the current device, or its allocation is too small";
     case FA_ERR_ALIAS: return "an output overlaps an input or the other output";
     case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case FA_ERR_WORKSPACE: return "the split-KV workspace is missing or smaller than fa_fwd_splitkv_workspace_bytes()";
   }
   return "unknown status";
 }

@@ -88,19 +88,42 @@ static_assert(Layout<64>::SMEM_BYTES <= MAX_SMEM_PER_CTA && Layout<128>::SMEM_BY
 
 struct Unit {
   int bh, qb;
-  int n0, n1;  // K/V tiles each query tile visits (0 = the tile lies past T)
+  int jb;      // first K/V tile of the unit (0 unless the key range is split)
+  int n0, n1;  // K/V tiles each query tile visits from jb (0 = nothing to do for that tile)
 };
 
-// Work item w -> (batch*head, 256-row query block).  Causal launches list the
-// longest query blocks first.
+// Work item w -> (batch*head, 256-row query block[, key split]).  Causal
+// launches list the longest query blocks first.  With split keys, split s of a
+// unit covers key tiles [s * split_tiles, (s + 1) * split_tiles) of what each
+// query tile may see.
+template <bool PARTIAL>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
   Unit u;
-  const int band = w / p.BH;
-  u.bh = w - band * p.BH;
+  int band, s = 0;
+  if (PARTIAL) {
+    const int per_band = p.BH * p.num_splits;
+    band = w / per_band;
+    const int rem = w - band * per_band;
+    s = rem / p.BH;
+    u.bh = rem - s * p.BH;
+  } else {
+    band = w / p.BH;
+    u.bh = w - band * p.BH;
+  }
   u.qb = p.causal ? (p.nqb - 1 - band) : band;
   const int q0 = u.qb * 2 * BM, q1 = q0 + BM;
-  u.n0 = (q0 >= p.T) ? 0 : (p.causal ? min(p.nk, q0 / BN + 1) : p.nk);
-  u.n1 = (q1 >= p.T) ? 0 : (p.causal ? min(p.nk, q1 / BN + 1) : p.nk);
+  const int e0 = (q0 >= p.T) ? 0 : (p.causal ? min(p.nk, q0 / BN + 1) : p.nk);  // tiles visible to tile 0
+  const int e1 = (q1 >= p.T) ? 0 : (p.causal ? min(p.nk, q1 / BN + 1) : p.nk);
+  if (PARTIAL) {
+    u.jb = s * p.split_tiles;
+    const int end = u.jb + p.split_tiles;
+    u.n0 = max(0, min(e0, end) - u.jb);
+    u.n1 = max(0, min(e1, end) - u.jb);
+  } else {
+    u.jb = 0;
+    u.n0 = e0;
+    u.n1 = e1;
+  }
   return u;
 }
 
@@ -151,7 +174,7 @@ __device__ __forceinline__ bool drain_all(const Waiter& W, uint32_t bar, uint32_
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-template <int D>
+template <int D, bool PARTIAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -231,8 +254,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       for (int k = 0; ok && k * G < p.num_units; ++k) {
         const int w = unit_of(k, blockIdx.x, G);
         if (w >= p.num_units) continue;
-        const Unit u = decode_unit(p, w);
+        const Unit u = decode_unit<PARTIAL>(p, w);
         const int nmax = max(u.n0, u.n1);
+        if (nmax == 0) continue;  // an empty key split: no role touches it
         const int qb = nu % L::QBUF;
         const uint32_t qpar = (nu / L::QBUF) & 1;
         if (!(ok = wait_all(W, bar_q_empty + 8 * qb, qpar ^ 1))) break;
@@ -252,7 +276,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           int k2 = k + 1, w2 = unit_of(k2, blockIdx.x, G);
           if (w2 >= p.num_units && (k2 + 1) * G < p.num_units) w2 = unit_of(++k2, blockIdx.x, G);
           if (w2 < p.num_units) {
-            const Unit u2 = decode_unit(p, w2);
+            const Unit u2 = decode_unit<PARTIAL>(p, w2);
             for (int i = 0; i < 2; ++i)
               if ((i ? u2.n1 : u2.n0) > 0)
                 for (int b = 0; b < L::BOXES; ++b)
@@ -266,7 +290,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_arrive_expect_tx_elect(bar_kv_full + 8 * stage, L::TILE_BYTES);
 #pragma unroll
             for (int b = 0; b < L::BOXES; ++b)
-              tma_load_3d_elect(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, kv == 0 ? &tmK : &tmV, b * 64, j * BN,
+              tma_load_3d_elect(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, kv == 0 ? &tmK : &tmV, b * 64, (u.jb + j) * BN,
                           u.bh, bar_kv_full + 8 * stage);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -305,8 +329,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       for (int k = 0; ok && k * G < p.num_units; ++k) {
         const int w = unit_of(k, blockIdx.x, G);
         if (w >= p.num_units) continue;
-        const Unit u = decode_unit(p, w);
+        const Unit u = decode_unit<PARTIAL>(p, w);
         const int n0 = u.n0, n1 = u.n1, nmax = max(n0, n1);
+        if (nmax == 0) continue;
         const int last_i = n1 > 0 ? 1 : 0;
         const int qb = nu % L::QBUF;
         if (!(ok = wait_all(W, bar_q_full + 8 * qb, (nu / L::QBUF) & 1))) break;
@@ -423,7 +448,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int k = 0; ok && k * G < p.num_units; ++k) {
       const int w = unit_of(k, blockIdx.x, G);
       if (w >= p.num_units) continue;
-      const Unit u = decode_unit(p, w);
+      const Unit u = decode_unit<PARTIAL>(p, w);
       const int n = i ? u.n1 : u.n0;
       if (n == 0) continue;
       const int q0 = u.qb * 2 * BM + i * BM;
@@ -437,7 +462,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tc_fence_after();
         uint32_t sr[BN];
         tmem_ld128_wait(t_s, sr);
-        const int k0 = j * BN;
+        const int k0 = (u.jb + j) * BN;
         if ((p.causal && k0 + BN - 1 > q0) || k0 + BN > p.T) {  // diagonal or ragged tail tile
           int lim = p.T - k0;
           if (p.causal) lim = min(lim, row - k0 + 1);
@@ -517,6 +542,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tc_fence_after();
       if (L::LR_IN_TMEM) lr = u2f(tmem_ld1_wait(t_o + D));  // sum p~ formed by the P V MMA
       const float inv_l = 1.f / lr;
+      if (PARTIAL) {  // this split's normalised output (fp32) and its LSE
+        const int s = u.jb / p.split_tiles;
+        const size_t prow = static_cast<size_t>(s) * p.BH * p.T + static_cast<size_t>(u.bh) * p.T + row;
+        float* orow = p.opart + prow * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32_wait(t_o + c * 32, ov);
+          if (row < p.T) {
+            float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(u2f(ov[4 * e]) * inv_l, u2f(ov[4 * e + 1]) * inv_l, u2f(ov[4 * e + 2]) * inv_l,
+                                   u2f(ov[4 * e + 3]) * inv_l);
+          }
+        }
+        if (row < p.T) p.lsepart[prow] = (m_run + log2f(l)) * LN2;
+      } else {
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(u.bh) * p.T + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -532,6 +575,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
       if (row < p.T) p.lse[static_cast<size_t>(u.bh) * p.T + row] = (m_run + log2f(l)) * LN2;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(my_o_empty);
@@ -564,7 +608,7 @@ __global__ void fa_wait_selftest_kernel(unsigned long long timeout_ns) {
 
 // ---------------------------------------------------------------- host side
 
-template <int D>
+template <int D, bool PARTIAL>
 static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                           int grid, cudaStream_t stream) {
   static bool attr_set[64] = {};
@@ -572,7 +616,8 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(fa_fwd_kernel<D, PARTIAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -581,13 +626,81 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = Layout<D>::SMEM_BYTES;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D>, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL>, q, k, v, p);
 }
 
 cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const Params& p, int grid, cudaStream_t stream) {
-  if (d == 64) return launch<64>(q, k, v, p, grid, stream);
-  return launch<128>(q, k, v, p, grid, stream);
+  if (d == 64) return launch<64, false>(q, k, v, p, grid, stream);
+  return launch<128, false>(q, k, v, p, grid, stream);
+}
+
+cudaError_t launch_fa_fwd_partial(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                  const Params& p, int grid, cudaStream_t stream) {
+  if (d == 64) return launch<64, true>(q, k, v, p, grid, stream);
+  return launch<128, true>(q, k, v, p, grid, stream);
+}
+
+// Merge of the per-split partials of every row ("FlashAttention and Fused
+// Kernels", section "Flash-Decoding": each split's output is weighted by its
+// log-sum-exp): with M = max_s LSE_s and w_s = e^(LSE_s - M),
+//   O = sum_s w_s O_s / sum_s w_s,   LSE = M + ln sum_s w_s.
+// A split contributes to row t when its first key is visible to t (causal) or
+// lies before T.  One warp per row; lane c owns D/32 contiguous columns.
+template <int D>
+__global__ void __launch_bounds__(256) fa_split_combine_kernel(const Params p) {
+  constexpr int CPL = D / 32;  // columns per lane
+  const int lane = threadIdx.x % 32;
+  const size_t rows = static_cast<size_t>(p.BH) * p.T;
+  const size_t warps = gridDim.x * (blockDim.x / 32);
+  const int tiles_total = (p.nk + p.split_tiles - 1) / p.split_tiles;
+  for (size_t r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < rows; r += warps) {
+    const int t = static_cast<int>(r % p.T);
+    int ns = min(p.num_splits, tiles_total);
+    if (p.causal) ns = min(ns, t / (BN * p.split_tiles) + 1);
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, p.lsepart[s * rows + r]);
+    float acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    float wsum = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float w = expf(p.lsepart[s * rows + r] - M);
+      wsum += w;
+      const float* src = p.opart + (s * rows + r) * D + lane * CPL;
+      if (CPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2 % CPL] += w * v.z;
+        acc[3 % CPL] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
+    const float inv = 1.f / wsum;
+    __nv_bfloat16* dst = p.o + r * D + lane * CPL;
+    if (CPL == 4) {
+      uint2 pk = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2 % CPL] * inv, acc[3 % CPL] * inv));
+      *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0) p.lse[r] = M + logf(wsum);
+  }
+}
+
+cudaError_t launch_split_combine(int d, const Params& p, int num_sms, cudaStream_t stream) {
+  const size_t rows = static_cast<size_t>(p.BH) * p.T;
+  const size_t blocks_needed = (rows + 7) / 8;
+  const int grid = static_cast<int>(blocks_needed < static_cast<size_t>(num_sms) * 8 ? blocks_needed : num_sms * 8);
+  if (d == 64)
+    fa_split_combine_kernel<64><<<grid, 256, 0, stream>>>(p);
+  else
+    fa_split_combine_kernel<128><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t stream) {

@@ -17,10 +17,20 @@ struct Params {
   int num_units;              // BH * nqb
   float scale_log2;           // scale * log2(e)
   unsigned long long timeout_ns;  // bound on every in-kernel wait
+  // split-KV (partial) launches only: each row's key tiles are cut into
+  // num_splits ranges of split_tiles tiles; unit w -> (band, split, bh)
+  int num_splits;             // 1 for a plain launch
+  int split_tiles;            // key tiles per split (>= 1)
+  float* opart;               // [num_splits][BH*T][d] fp32 partial outputs (normalised)
+  float* lsepart;             // [num_splits][BH*T] fp32 partial LSE (natural log)
 };
 
 cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const Params& p, int grid, cudaStream_t stream);
+// The same kernel writing per-split partials (p.opart, p.lsepart), then the merge.
+cudaError_t launch_fa_fwd_partial(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                  const Params& p, int grid, cudaStream_t stream);
+cudaError_t launch_split_combine(int d, const Params& p, int num_sms, cudaStream_t stream);
 int fa_fwd_smem_bytes(int d);
 int fa_fwd_threads();
 int fa_fwd_rows_per_unit();

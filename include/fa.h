@@ -39,6 +39,7 @@
 #define FA_GB300_FA_H
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -57,8 +58,12 @@ typedef enum {
   FA_ERR_BAD_ARG = 9,               /* an argument is out of range (causal not 0 or 1, a self-test timeout) */
   FA_ERR_BAD_POINTER = 10,          /* a pointer is not device memory, or its allocation is too small */
   FA_ERR_ALIAS = 11,                /* O or LSE overlaps an input or each other */
-  FA_ERR_CUDA = 12                  /* a CUDA runtime or driver query failed */
+  FA_ERR_CUDA = 12,                 /* a CUDA runtime or driver query failed */
+  FA_ERR_WORKSPACE = 13             /* the split-KV workspace is missing or too small */
 } fa_status;
+
+/* Largest number of key splits fa_fwd_splitkv accepts. */
+#define FA_MAX_SPLITS 256
 
 /*
  * Attention forward.
@@ -74,6 +79,32 @@ typedef enum {
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int H, int T, int d, int causal, float scale,
                  cudaStream_t stream);
+
+/*
+ * Attention forward with the keys of every row split into ranges that run as
+ * separate work units (Flash-Decoding: "FlashAttention and Fused Kernels:
+ * Attention Without the n x n Matrix", section "Flash-Decoding: split the
+ * cache, not the queries").  Each unit writes its range's normalised output
+ * (fp32) and log-sum-exp into `workspace`; a second kernel on the same stream
+ * merges them, weighting each split by its log-sum-exp.  O and LSE are the
+ * same quantities fa_fwd computes (up to rounding).
+ *   q .. scale, stream : as for fa_fwd.
+ *   num_splits : 1 .. FA_MAX_SPLITS; the keys (ceil(T / 128) tiles of 128) are
+ *                cut into ceil(tiles / ceil(tiles / num_splits)) ranges of
+ *                equal tile count.
+ *   workspace  : caller-owned device memory of at least
+ *                fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) bytes,
+ *                16-byte aligned, not overlapping any tensor argument.  Its
+ *                contents are scratch: overwritten, never read before written.
+ * Errors: as fa_fwd, plus FA_ERR_BAD_ARG (num_splits out of range) and
+ * FA_ERR_WORKSPACE (NULL or too small a workspace).
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int T, int d, int causal, float scale, int num_splits,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes fa_fwd_splitkv needs (0 for invalid sizes): num_splits * B*H*T * (d + 1) * 4, rounded up to 256. */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int T, int d, int num_splits);
 
 /* A static, human-readable name for a status code. */
 const char* fa_status_string(fa_status s);
