@@ -40,6 +40,8 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 SWEEP_DEFAULT = ["tiny_causal_b1h4t256d64", "gpt2m_b16h16t1024d64", "gpt2m_stress_b16h16t1024d64",
                  "llama8b_causal_b1h32t4096d128", "llama8b_b1h32t4096d128", "long_causal_b1h32t32768d128"]
+# split-KV (fa_fwd_splitkv) entries of the sweep: workload -> key splits
+SPLITKV_SWEEP = {"tiny_causal_b1h4t256d64": 2, "gpt2s_causal_b8h12t1024d64": 2, "llama8b_b1h32t4096d128": 2}
 
 
 def metric_flops(B, H, T, d, causal):
@@ -315,9 +317,39 @@ def run_e2e(fa, torch, dev, w, qkv, scale, steps, pg):
             "path": "exact_io_aware_07_gb300.attention() with pinned host buffers"}
 
 
-def run_sweep(fa, torch, dev, names, peaks):
+def time_splitkv(fa, torch, dev, w, qkv, scale, num_splits, steps):
+    """Device time of fa_fwd_splitkv (both kernels) per step, inputs rotating past L2."""
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    sets, stream, ev, start, end, nsets = time_kernel(fa, torch, dev, w, qkv, steps, 0, scale, True)
+    ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits), dtype=torch.uint8, device=dev)
+    for i in range(5):
+        q, k, v, o, lse = sets[i % nsets]
+        fa.fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, ws, stream)
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        q, k, v, o, lse = sets[i % nsets]
+        ev[i][0].record(stream)
+        fa.fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, ws, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return sum(ms) / len(ms) / 1e3, ws.numel()
+
+
+def run_sweep(fa, torch, dev, names, peaks, splitkv=SPLITKV_SWEEP):
     """Every other workload, measured the same way with fewer steps (informational)."""
     out = {}
+    for name, ns in splitkv.items():
+        w = fi.WORKLOADS[name]
+        qkv = fi.make_qkv(w["B"], w["H"], w["T"], w["d"], seed=0, sigma_qk=w["sigma_qk"])
+        f = metric_flops(w["B"], w["H"], w["T"], w["d"], w["causal"])
+        steps = int(min(2000, max(20, 0.5 / max(f / 1.0e15, 1e-6))))
+        sec, ws_bytes = time_splitkv(fa, torch, dev, w, qkv, 1.0 / math.sqrt(w["d"]), ns, steps)
+        out[f"splitkv{ns}_{name}"] = {"ms_mean": round(sec * 1e3, 4), "tflops": round(f / sec / 1e12, 1),
+                                      "pct_of_bf16_peak": round(100 * f / sec / 1e12 / peaks["bf16_tflops"], 1),
+                                      "steps": steps, "workspace_bytes": ws_bytes,
+                                      "kernels": "fa_fwd_kernel (partial) + fa_split_combine_kernel"}
+        torch.cuda.empty_cache()
     for name in names:
         w = fi.WORKLOADS[name]
         B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]

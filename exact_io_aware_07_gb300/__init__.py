@@ -9,6 +9,7 @@ the library has not been built, importing works but the first call raises.
 Entry points (same names as the C ABI):
     fa_fwd(q, k, v, o, lse, causal, scale, stream=None)
     fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, workspace, stream=None)
+    fa_fwd_splitkv_noalloc(q, k, v, o, lse, causal, scale, num_splits, stream=None)
     fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits)
     fa_status_string(code), fa_device_status(stream=None), fa_selftest_wait_timeout(us, stream=None)
     fa_fwd_launch_shape(B, H, T, d, causal, num_sms), fa_version()
@@ -25,7 +26,8 @@ import os
 from ._build import build, lib_path  # noqa: F401
 
 __all__ = [
-    "FAError", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_status_string", "fa_device_status",
+    "FAError", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
+    "fa_status_string", "fa_device_status", "FA_NOALLOC_SCRATCH_BYTES",
     "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version",
     "attention", "attention_splitkv", "load_library", "STATUS", "FA_MAX_SPLITS",
 ]
@@ -37,8 +39,9 @@ STATUS = {
     11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA", 13: "FA_ERR_WORKSPACE",
 }
 FA_MAX_SPLITS = 256
-EXPORTED = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_status_string", "fa_device_status",
-            "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version"]
+EXPORTED = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
+            "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version"]
+FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class FAError(RuntimeError):
@@ -73,6 +76,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd_launch_shape.restype = i
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_splitkv_noalloc.restype = i
     lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
@@ -208,3 +213,17 @@ def attention_splitkv(q, k, v, causal: bool = False, num_splits: int = 2, scale:
     ws = torch.empty(fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits), dtype=torch.uint8, device=q.device)
     fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, ws, stream)
     return o, lse
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, causal: bool, scale: float, num_splits: int, stream=None) -> None:
+    """Split-KV attention with the library's fixed device scratch (no workspace, no allocation).
+
+    For callers that cannot allocate device memory while running; see the
+    declaration in include/fa.h for the size limit and the sharing rules.
+    """
+    B, H, T, d = _check_qkv_o_lse(q, k, v, o, lse)
+    code = load_library().fa_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                 lse.data_ptr(), B, H, T, d, int(bool(causal)), float(scale),
+                                                 int(num_splits), ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_fwd_splitkv_noalloc")

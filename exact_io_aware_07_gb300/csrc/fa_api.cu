@@ -252,6 +252,21 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   return FA_OK;
 }
 
+fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                 int T, int d, int causal, float scale, int num_splits, cudaStream_t stream) {
+  if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_BAD_ARG;
+  Prepared pr;
+  fa_status st = prepare(q, k, v, o, lse, B, H, T, d, causal, scale, &pr);
+  if (st != FA_OK) return st;
+  if (fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (fa::noalloc_scratch_address(pr.dev, &scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return launch_splitkv(pr, d, num_splits, static_cast<float*>(scratch), stream);
+}
+
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int T, int d, int num_splits) {
   if (B < 1 || H < 1 || T < 1 || (d != 64 && d != 128) || num_splits < 1 || num_splits > FA_MAX_SPLITS) return 0;
   const size_t rows = static_cast<size_t>(B) * H * T;
@@ -276,6 +291,8 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   if (overlaps(workspace, need, lse, lse_bytes)) return FA_ERR_ALIAS;
   return launch_splitkv(pr, d, num_splits, static_cast<float*>(workspace), stream);
 }
+
+static_assert(FA_NOALLOC_SCRATCH_BYTES == fa::kNoAllocScratchBytes, "fa.h and the kernel disagree on the scratch size");
 
 const char* fa_status_string(fa_status s) {
   switch (s) {

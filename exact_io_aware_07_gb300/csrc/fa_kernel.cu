@@ -44,6 +44,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "fa_kernel.h"
 #include "ptx.cuh"
 
@@ -701,6 +703,29 @@ cudaError_t launch_split_combine(int d, const Params& p, int num_sms, cudaStream
   else
     fa_split_combine_kernel<128><<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- fixed scratch (no allocation)
+// Scratch for fa_fwd_splitkv_noalloc: a device global, so the library never
+// allocates for that entry point.  Every device that loads the library holds
+// one copy of it until the process exits.  In host code `g_noalloc_scratch`
+// names a host-side stand-in, not device memory: its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+cudaError_t noalloc_scratch_address(int dev, void** out) {
+  static void* addr[64] = {};
+  static std::mutex mu;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // the current device is `dev`
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t stream) {

@@ -37,4 +37,10 @@ int fa_fwd_rows_per_unit();
 cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* out);
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t stream);
 
+// Size of the fixed device scratch behind fa_fwd_splitkv_noalloc (32 MiB).
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+// Device address of that scratch on device `dev` (must be the current device);
+// looked up on the first call for each device, then cached.
+cudaError_t noalloc_scratch_address(int dev, void** out);
+
 }  // namespace fa

@@ -103,6 +103,38 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
                          int B, int H, int T, int d, int causal, float scale, int num_splits,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the fixed device scratch fa_fwd_splitkv_noalloc uses (32 MiB). */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * fa_fwd_splitkv without a workspace argument and without any allocation.
+ * (Not part of the method described on the pages; an interface addition.)
+ *
+ * For callers that cannot allocate device memory while they run: code whose
+ * device memory is owned by a framework's pool or a fixed budget, plugins
+ * that must not call the CUDA allocator, or hosts where an allocation at that
+ * point would block or fail.  The split partials go to a fixed scratch array
+ * of FA_NOALLOC_SCRATCH_BYTES that the library holds on every device it is
+ * loaded on (for the life of the process); nothing calls cudaMalloc, cudaFree
+ * or any other allocating routine.
+ *
+ * Arguments and results are those of fa_fwd_splitkv minus the workspace.
+ * Limits and behaviour:
+ *   - fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) must not exceed
+ *     FA_NOALLOC_SCRATCH_BYTES, else FA_ERR_WORKSPACE and nothing runs;
+ *   - the first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on that device;
+ *   - every call on a device shares the one scratch array, which keeps what
+ *     the last call left there.  Nothing in it needs to start at zero: each
+ *     call writes every partial before its merge reads it.  Calls whose
+ *     kernels overlap on the GPU (different streams without ordering between
+ *     them) race on the scratch and give wrong results; order them.
+ */
+fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int T, int d, int causal, float scale, int num_splits,
+                                 cudaStream_t stream);
+
 /* Workspace bytes fa_fwd_splitkv needs (0 for invalid sizes): num_splits * B*H*T * (d + 1) * 4, rounded up to 256. */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int T, int d, int num_splits);
 
