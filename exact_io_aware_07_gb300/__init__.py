@@ -39,7 +39,7 @@ STATUS = {
     11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA", 13: "FA_ERR_WORKSPACE",
 }
 FA_MAX_SPLITS = 256
-EXPORTED = ["fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
+EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
             "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version"]
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -68,6 +68,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd_gqa.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -154,6 +156,40 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
                       B, H, T, d, int(bool(causal)), float(scale), ctypes.c_void_p(_stream_handle(stream)))
     if code:
         raise FAError(code, "fa_fwd")
+
+
+def fa_fwd_gqa(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """Grouped K/V heads: q, o (B, H, T, d) and k, v (B, Hkv, T, d) bf16, H a multiple of Hkv;
+    query head h reads K/V head h // (H // Hkv).  lse: fp32 (B, H, T)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 4-D tensor")
+    B, H, T, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(o.shape) != (B, H, T, d) or tuple(k.shape) != (B, Hkv, T, d) or k.shape != v.shape:
+        raise ValueError("q, o must be (B, H, T, d) and k, v (B, Hkv, T, d)")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 (B, H, T) tensor")
+    code = load_library().fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                     B, H, Hkv, T, d, int(bool(causal)), float(scale),
+                                     ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_fwd_gqa")
+
+
+def attention_gqa(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocates O and LSE and runs ``fa_fwd_gqa``; ``scale`` defaults to 1/sqrt(d)."""
+    import torch
+
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    fa_fwd_gqa(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):

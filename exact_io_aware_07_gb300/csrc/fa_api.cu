@@ -179,28 +179,40 @@ struct Prepared {
 };
 
 // Validation shared by the entry points, then the TMA descriptors and the
-// launch parameters of a plain (unsplit) launch.
-fa_status prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int d,
-                  int causal, float scale, Prepared* pr) {
+// launch parameters of a plain (unsplit) launch.  K and V hold Hkv heads per
+// batch entry; H query heads share them in groups of H / Hkv (Hkv == H: one K/V
+// head per query head).
+fa_status prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int T,
+                  int d, int causal, float scale, Prepared* pr) {
   fa_status st = validate_host(q, k, v, o, lse, B, H, T, d, causal, scale);
   if (st != FA_OK) return st;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_BAD_SHAPE;
   if ((st = current_device(&pr->dev, &pr->num_sms)) != FA_OK) return st;
-  const int BH = B * H;
-  const size_t qkv_bytes = static_cast<size_t>(BH) * T * d * 2;
+  const int BH = B * H, BHkv = B * Hkv;
+  const size_t q_bytes = static_cast<size_t>(BH) * T * d * 2;
+  const size_t kv_bytes = static_cast<size_t>(BHkv) * T * d * 2;
   const size_t lse_bytes = static_cast<size_t>(BH) * T * 4;
-  for (const void* x : {q, k, v, static_cast<const void*>(o)})
-    if ((st = check_device_range(x, qkv_bytes, pr->dev)) != FA_OK) return st;
+  for (const void* x : {q, static_cast<const void*>(o)})
+    if ((st = check_device_range(x, q_bytes, pr->dev)) != FA_OK) return st;
+  for (const void* x : {k, v})
+    if ((st = check_device_range(x, kv_bytes, pr->dev)) != FA_OK) return st;
   if ((st = check_device_range(lse, lse_bytes, pr->dev)) != FA_OK) return st;
-  for (const void* in : {q, k, v})
-    if (overlaps(o, qkv_bytes, in, qkv_bytes) || overlaps(lse, lse_bytes, in, qkv_bytes)) return FA_ERR_ALIAS;
-  if (overlaps(o, qkv_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
-  if (!make_tensor_map(&pr->tq, q, BH, T, d) || !make_tensor_map(&pr->tk, k, BH, T, d) ||
-      !make_tensor_map(&pr->tv, v, BH, T, d))
+  const struct {
+    const void* p;
+    size_t n;
+  } inputs[3] = {{q, q_bytes}, {k, kv_bytes}, {v, kv_bytes}};
+  for (const auto& in : inputs)
+    if (overlaps(o, q_bytes, in.p, in.n) || overlaps(lse, lse_bytes, in.p, in.n)) return FA_ERR_ALIAS;
+  if (overlaps(o, q_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
+  if (!make_tensor_map(&pr->tq, q, BH, T, d) || !make_tensor_map(&pr->tk, k, BHkv, T, d) ||
+      !make_tensor_map(&pr->tv, v, BHkv, T, d))
     return FA_ERR_CUDA;
   fa::Params& p = pr->p;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.BH = BH;
+  p.H = H;
+  p.group = H / Hkv;
   p.T = T;
   p.causal = causal;
   p.nqb = (T + 255) / 256;
@@ -241,8 +253,13 @@ extern "C" {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int d,
                  int causal, float scale, cudaStream_t stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, T, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int T,
+                     int d, int causal, float scale, cudaStream_t stream) {
   Prepared pr;
-  fa_status st = prepare(q, k, v, o, lse, B, H, T, d, causal, scale, &pr);
+  fa_status st = prepare(q, k, v, o, lse, B, H, Hkv, T, d, causal, scale, &pr);
   if (st != FA_OK) return st;
   const int grid = pr.p.num_units < pr.num_sms ? pr.p.num_units : pr.num_sms;
   if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, pr.p, grid, stream) != cudaSuccess) {
@@ -256,7 +273,7 @@ fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, vo
                                  int T, int d, int causal, float scale, int num_splits, cudaStream_t stream) {
   if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_BAD_ARG;
   Prepared pr;
-  fa_status st = prepare(q, k, v, o, lse, B, H, T, d, causal, scale, &pr);
+  fa_status st = prepare(q, k, v, o, lse, B, H, H, T, d, causal, scale, &pr);
   if (st != FA_OK) return st;
   if (fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
@@ -279,7 +296,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
                          cudaStream_t stream) {
   if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_BAD_ARG;
   Prepared pr;
-  fa_status st = prepare(q, k, v, o, lse, B, H, T, d, causal, scale, &pr);
+  fa_status st = prepare(q, k, v, o, lse, B, H, H, T, d, causal, scale, &pr);
   if (st != FA_OK) return st;
   const size_t need = fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
@@ -334,7 +351,7 @@ fa_status fa_fwd_launch_shape(int B, int H, int T, int d, int causal, int num_sm
   if (num_sms < 1) return FA_ERR_BAD_ARG;
   const long long units = static_cast<long long>(B) * H * ((T + 255) / 256);
   *grid = static_cast<int>(units < num_sms ? units : num_sms);
-  *threads = fa::fa_fwd_threads();
+  *threads = fa::fa_fwd_threads(d);
   *smem_bytes = fa::fa_fwd_smem_bytes(d);
   return FA_OK;
 }

@@ -19,27 +19,27 @@
 // multiplies by, and O = sum p~ v / lr is a convex combination of the value
 // rows under exactly the weights used (a row dominated by one key returns that
 // key's value row unchanged, whatever the stale m); l sums the fp32 weights and
-// gives the LSE without the bf16 rounding of the weights.  At d = 64 the tensor
-// core forms lr: each V tile is extended, inside the MMA operand, by 16 columns
-// of ones (a constant shared-memory block reached through the descriptor's
-// leading-byte offset), so O's column 64 accumulates sum p~ with the same
-// arithmetic as the numerator, at no MMA cost (N = 80 runs as fast as N = 64).
-// At d = 128 Tensor Memory has no room for the extra columns and the softmax
-// threads sum the packed weights.
+// gives the LSE without the bf16 rounding of the weights.
 //
-// Roles (320 threads, one CTA per SM, persistent over work units):
+// Roles (one CTA per SM, persistent over work units):
 //   warps 0-3  softmax for query tile 0 of the unit (one TMEM lane = one row per thread)
 //   warps 4-7  softmax for query tile 1
 //   warp 8     TMA producer: Q tiles once per unit, then K_j, V_j through a ring
-//   warp 9     TMEM allocator and tcgen05.mma issuer
-// Warps 8 and 9 run their schedules on all 32 lanes (every operand stays
-// warp-uniform); elect.sync inside each TMA, MMA and commit picks the one lane
-// that issues it.
+//   warp 9     Tensor Memory allocator; tcgen05.mma issuer (d = 128: both tiles;
+//              d = 64: tile 0)
+//   warp 10    d = 64 only: tcgen05.mma issuer for tile 1 (warp 11 only joins the
+//              final barrier; 384 threads at d = 64, 320 at d = 128)
+// The issuing warps run their schedules on all 32 lanes (every operand stays
+// warp-uniform); elect.sync inside each TMA, MMA and commit picks the lane that
+// issues it.
 // A work unit is (batch*head, 256 query rows) = two 128-row query tiles that
-// share every K/V tile loaded.  Tensor Memory (512 columns):
+// share every K/V tile loaded.  Tensor Memory (512 columns, fp32):
 //   S_0 [0,128)  S_1 [128,256)  O_0 [256,256+d)  O_1 [256+d,256+2d)
-// P_i (bf16 pairs) is written over the first 64 columns of S_i once S_i has
-// been read; the MMA that next writes S_i is issued after the one reading P_i.
+// d = 128: P_i (bf16 pairs) is written over the first 64 columns of S_i once S_i
+// has been read, so S_i(j+1) waits for P_i(j) V_j.  d = 64: P_0 [384,448) and
+// P_1 [448,512) have columns of their own, so S_i(j+1) is computed while the
+// softmax of S_i(j) runs, and each tile's MMAs are issued by a warp of its own
+// that waits only on that tile's barriers.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,13 +49,14 @@
 #include "fa_kernel.h"
 #include "ptx.cuh"
 
+
 namespace fa {
 
 constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 128;          // keys per tile
-constexpr int NUM_THREADS = 320;
 constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int MMA_WARP0 = 9;   // MMA issuer for query tile 0; also allocates Tensor Memory
+constexpr int MMA_WARP1 = 10;  // MMA issuer for query tile 1 (warp 11 only joins the final barrier)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16, 128-byte swizzle
 constexpr float LN2 = 0.693147180559945309f;
@@ -72,17 +73,27 @@ struct Layout {
   static constexpr int STAGES = (D == 128) ? 4 : 6;   // K/V ring depth (tiles)
   static constexpr int Q_OFF = 0;                      // [QBUF units][2 query tiles]
   static constexpr int KV_OFF = QBUF * 2 * TILE_BYTES;
-  static constexpr bool LR_IN_TMEM = (D == 64);          // the P V MMA also forms sum p~ (see above)
-  static constexpr int ON = LR_IN_TMEM ? D + 16 : D;     // O columns per query tile in TMEM
-  static constexpr int ONES_OFF = KV_OFF + STAGES * TILE_BYTES;   // 128 x 64 bf16 ones (d = 64 only)
-  static constexpr int BAR_OFF = ONES_OFF + (LR_IN_TMEM ? BOX_BYTES : 0);
-  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2], done
-  static constexpr int NUM_BARS = 4 + 2 * STAGES + 8 + 1;
+  // d = 64: P_i has Tensor Memory columns of its own, so S_i(j+1) may be computed
+  // while the softmax of S_i(j) runs (see the MMA issuer); d = 128: P_i overwrites S_i.
+  static constexpr bool SEP_P = (D == 64);
+  static constexpr int ON = D;                          // O columns per query tile in TMEM
+  // d = 64: one MMA-issuing warp per query tile (warps 9, 10; warp 11 idle); d = 128: warp 9 alone
+  static constexpr int THREADS = SEP_P ? 384 : 320;
+  static constexpr int MMA_WARPS = SEP_P ? 2 : 1;
+  static constexpr int BAR_OFF = KV_OFF + STAGES * TILE_BYTES;
+  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2],
+  // s_free[2], done
+  static constexpr int NUM_BARS = 4 + 2 * STAGES + 10 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // TMEM base slot, abort flag
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
   static __device__ __forceinline__ constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
   static __device__ __forceinline__ constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * ON; }
+  // where P_i lives: its own 64 columns after O_1, or the first 64 columns of S_i
+  static __device__ __forceinline__ constexpr uint32_t p_col(int i) {
+    return SEP_P ? 256u + 2u * ON + uint32_t(i) * 64u : s_col(i);
+  }
 };
+static_assert(!Layout<64>::SEP_P || 256 + 2 * Layout<64>::ON + 128 <= 512, "Tensor Memory columns exceed 512");
 
 constexpr int MAX_SMEM_PER_CTA = 232448;  // 227 KB opt-in dynamic shared memory per block on sm_103
 static_assert(Layout<64>::SMEM_BYTES <= MAX_SMEM_PER_CTA && Layout<128>::SMEM_BYTES <= MAX_SMEM_PER_CTA,
@@ -177,7 +188,7 @@ __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
 template <int D, bool PARTIAL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Layout<D>::THREADS, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const Params p) {
   using L = Layout<D>;
@@ -197,7 +208,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t bar_p_full = barx + 16;   // [2]
   const uint32_t bar_o_full = barx + 32;   // [2]
   const uint32_t bar_o_empty = barx + 48;  // [2]
-  const uint32_t bar_done = barx + 64;
+  const uint32_t bar_s_free = barx + 64;   // [2] (SEP_P: S_i has been read into registers)
+  const uint32_t bar_done = barx + 80;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
 
@@ -208,29 +220,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_q_full + 8 * b, 1);
-      mbar_init(bar_q_empty + 8 * b, 1);
+      mbar_init(bar_q_empty + 8 * b, L::MMA_WARPS);  // one release per MMA-issuing warp
     }
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(bar_kv_full + 8 * s, 1);
-      mbar_init(bar_kv_empty + 8 * s, 1);
+      mbar_init(bar_kv_empty + 8 * s, L::MMA_WARPS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s_full + 8 * i, 1);
       mbar_init(bar_p_full + 8 * i, 4);
       mbar_init(bar_o_full + 8 * i, 1);
       mbar_init(bar_o_empty + 8 * i, 4);
+      mbar_init(bar_s_free + 8 * i, 4);
     }
-    mbar_init(bar_done, 1);
+    mbar_init(bar_done, L::MMA_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (L::LR_IN_TMEM) {  // the ones block read by the P V MMA (bf16 1.0 everywhere, so swizzle is moot)
-    uint4* ones = reinterpret_cast<uint4*>(smem + L::ONES_OFF);
-    for (int x = threadIdx.x; x < BOX_BYTES / 16; x += NUM_THREADS)
-      ones[x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == MMA_WARP) {
+  if (warp == MMA_WARP0) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
@@ -259,6 +266,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const Unit u = decode_unit<PARTIAL>(p, w);
         const int nmax = max(u.n0, u.n1);
         if (nmax == 0) continue;  // an empty key split: no role touches it
+        // the K/V head this query head reads (query heads share K/V heads in groups)
+        const int kvh = p.group == 1 ? u.bh : (u.bh / p.H) * (p.H / p.group) + (u.bh % p.H) / p.group;
         const int qb = nu % L::QBUF;
         const uint32_t qpar = (nu / L::QBUF) & 1;
         if (!(ok = wait_all(W, bar_q_empty + 8 * qb, qpar ^ 1))) break;
@@ -285,23 +294,38 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                   tma_prefetch_l2_3d_elect(&tmQ, b * 64, u2.qb * 2 * BM + i * BM, u2.bh);
           }
         }
-        for (int j = 0; ok && j < nmax; ++j) {
-#pragma unroll
-          for (int kv = 0; kv < 2; ++kv) {
-            if (!(ok = wait_all(W, bar_kv_empty + 8 * stage, phase ^ 1))) break;
-            mbar_arrive_expect_tx_elect(bar_kv_full + 8 * stage, L::TILE_BYTES);
-#pragma unroll
-            for (int b = 0; b < L::BOXES; ++b)
-              tma_load_3d_elect(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, kv == 0 ? &tmK : &tmV, b * 64, (u.jb + j) * BN,
-                          u.bh, bar_kv_full + 8 * stage);
-            issued |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-            if (++stage == L::STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
+        // ring order = the order the MMA warps take tiles in: K_0 V_0 K_1 V_1 ..., or with
+        // separate P buffers K_0 K_1 V_0 K_2 V_1 K_3 ... V_(n-2) V_(n-1) (S runs a step ahead)
+#define FA_LOAD(kv, j)                                                                                    \
+  {                                                                                                       \
+    if (!(ok = wait_all(W, bar_kv_empty + 8 * stage, phase ^ 1))) break;                                  \
+    mbar_arrive_expect_tx_elect(bar_kv_full + 8 * stage, L::TILE_BYTES);                                  \
+    _Pragma("unroll") for (int b = 0; b < L::BOXES; ++b)                                                  \
+      tma_load_3d_elect(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, (kv) == 0 ? &tmK : &tmV, b * 64, \
+                        (u.jb + (j)) * BN, kvh, bar_kv_full + 8 * stage);                                 \
+    issued |= 1u << stage;                                                                                \
+    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);                                  \
+    if (++stage == L::STAGES) {                                                                           \
+      stage = 0;                                                                                          \
+      phase ^= 1;                                                                                         \
+    }                                                                                                     \
+  }
+        if (L::SEP_P) {
+          do {
+            FA_LOAD(0, 0);
+            if (nmax > 1) FA_LOAD(0, 1);
+          } while (0);
+          for (int j = 0; ok && j < nmax; ++j) {
+            FA_LOAD(1, j);
+            if (j + 2 < nmax) FA_LOAD(0, j + 2);
+          }
+        } else {
+          for (int j = 0; ok && j < nmax; ++j) {
+            FA_LOAD(0, j);
+            FA_LOAD(1, j);
           }
         }
+#undef FA_LOAD
       }
       if (!ok) {  // let every copy already issued land before the CTA exits
         for (int b = 0; b < 2; ++b)
@@ -311,16 +335,153 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       }
     }
     __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer (whole warp, one lane issues)
+  } else if (L::SEP_P && (warp == MMA_WARP0 || warp == MMA_WARP1)) {
+    // ------------------------------------------------------------ MMA issuers, one warp per query tile (SEP_P)
+    // Each warp runs its tile's schedule on all 32 lanes and elects one lane per MMA.  Both
+    // warps walk the whole K/V ring in the producer's order and release every stage (and
+    // the unit's Q buffer) whether or not their tile used it, so kv_empty and q_empty
+    // complete after two arrivals.
+    {
+      const int i = warp - MMA_WARP0;  // query tile of this warp
+      constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);   // S = Q K^T: both K-major
+      constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, L::ON, 1);  // O += P V: V is MN-major
+      // Descriptor halves: the address field (low 14 bits, in 16-byte units) is the
+      // only part that changes, and every offset added below stays inside it.
+      const uint64_t dqk = make_sdesc_sw128(sbase, 16, 1024);        // K-major tiles (Q, K)
+      const uint64_t dvv = make_sdesc_sw128(sbase, BOX_BYTES, 1024);  // MN-major V tiles
+      const uint32_t dqk_lo = uint32_t(dqk), dqk_hi = uint32_t(dqk >> 32);
+      const uint32_t dv_lo = uint32_t(dvv), dv_hi = uint32_t(dvv >> 32);
+      const uint32_t my_s_full = bar_s_full + 8 * i, my_p_full = bar_p_full + 8 * i;
+      const uint32_t my_o_full = bar_o_full + 8 * i, my_o_empty = bar_o_empty + 8 * i;
+      const uint32_t my_s_free = bar_s_free + 8 * i;
+      const uint32_t d_s = tmem + L::s_col(i), d_o = tmem + L::o_col(i), a_p = tmem + L::p_col(i);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pf = 0, oe = 0, sfr = 0;
+      bool ok = true;
+      int nu = 0;
+      for (int k = 0; ok && k * G < p.num_units; ++k) {
+        const int w = unit_of(k, blockIdx.x, G);
+        if (w >= p.num_units) continue;
+        const Unit u = decode_unit<PARTIAL>(p, w);
+        const int n = i ? u.n1 : u.n0, nmax = max(u.n0, u.n1);
+        if (nmax == 0) continue;
+        const int qb = nu % L::QBUF;
+        if (!(ok = wait_all(W, bar_q_full + 8 * qb, (nu / L::QBUF) & 1))) break;
+        ++nu;
+        tc_fence_after();
+        const uint32_t a_q = dqk_lo + ((L::Q_OFF + (2 * qb + i) * L::TILE_BYTES) >> 4);
+        // S_i = Q_i K^T over d in steps of 16 (stage ks of the ring); after the tile's last S
+        // the Q buffer is released
+#define FA_ISSUE_S(ks, x)                                                                               \
+  {                                                                                                     \
+    const uint32_t b0 = dqk_lo + ((L::KV_OFF + (ks) * L::TILE_BYTES) >> 4);                             \
+    _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                             \
+      const uint32_t off = (((kk / 4) * BOX_BYTES + (kk % 4) * 32) >> 4);                               \
+      mma_ss_elect(d_s, a_q + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);                \
+    }                                                                                                   \
+    mma_commit_elect(my_s_full);                                                                        \
+    if ((x) + 1 == n) mma_commit_elect(bar_q_empty + 8 * qb);                                           \
+  }
+        // O_i (+)= P_i V over keys in steps of 16 (stage vs of the ring)
+#define FA_ISSUE_PV(vs, acc)                                                                            \
+  {                                                                                                     \
+    const uint32_t s16 = ((vs) * L::TILE_BYTES) >> 4;                                                   \
+    const uint32_t b0 = dv_lo + (L::KV_OFF >> 4) + s16;                                                 \
+    _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                              \
+      mma_ts_elect(d_o, a_p + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi, IDESC_PV, ((acc) || kk > 0) ? 1u : 0u); \
+  }
+#define FA_TAKE(slot)                                                      \
+  {                                                                        \
+    slot = stage;                                                          \
+    if (!(ok = wait_all(W, bar_kv_full + 8 * stage, phase))) break;        \
+    if (++stage == L::STAGES) {                                            \
+      stage = 0;                                                           \
+      phase ^= 1;                                                          \
+    }                                                                      \
+    tc_fence_after();                                                      \
+  }
+#define FA_WAIT(bar, par)                                       \
+  {                                                             \
+    if (!(ok = wait_all(W, bar, par))) break;                   \
+    par ^= 1;                                                   \
+    tc_fence_after();                                           \
+  }
+        {
+          // S runs one K/V step ahead of the softmax: S_i(x) is issued once the softmax
+          // has read S_i(x-1) (s_free); P_i(j) V_j once P_i(j) is written (p_full), with
+          // a commit to o_full that the softmax waits on before it overwrites P_i or
+          // rescales O_i, and at the end of the unit.  Ring order: K_0 K_1 V_0 K_2 V_1 ...
+          do {
+            int ks = 0;
+            FA_TAKE(ks);
+            if (n > 0) {
+              uint32_t par = sfr ^ 1;
+              FA_WAIT(my_s_free, par);
+              sfr ^= 1;
+              FA_ISSUE_S(ks, 0);
+            }
+            mma_commit_elect(bar_kv_empty + 8 * ks);
+            if (nmax > 1) {
+              FA_TAKE(ks);
+              if (n > 1) {
+                uint32_t par = sfr ^ 1;
+                FA_WAIT(my_s_free, par);
+                sfr ^= 1;
+                FA_ISSUE_S(ks, 1);
+              }
+              mma_commit_elect(bar_kv_empty + 8 * ks);
+            }
+          } while (0);
+          if (!ok) break;
+          for (int j = 0; j < nmax; ++j) {
+            int vs = 0;
+            FA_TAKE(vs);
+            if (j < n) {
+              if (j == 0) {
+                uint32_t par = oe ^ 1;
+                FA_WAIT(my_o_empty, par);
+                oe ^= 1;
+              }
+              FA_WAIT(my_p_full, pf);
+              FA_ISSUE_PV(vs, j > 0);
+              mma_commit_elect(my_o_full);
+            }
+            mma_commit_elect(bar_kv_empty + 8 * vs);
+            if (j + 2 < nmax) {
+              int ks = 0;
+              FA_TAKE(ks);
+              if (j + 2 < n) {
+                uint32_t par = sfr ^ 1;
+                FA_WAIT(my_s_free, par);
+                sfr ^= 1;
+                FA_ISSUE_S(ks, j + 2);
+              }
+              mma_commit_elect(bar_kv_empty + 8 * ks);
+            }
+          }
+        }
+        if (!ok) break;
+        if (n == 0) mma_commit_elect(bar_q_empty + 8 * qb);  // this tile had nothing to do in the unit
+#undef FA_ISSUE_S
+#undef FA_ISSUE_PV
+#undef FA_TAKE
+#undef FA_WAIT
+      }
+      // every MMA and every commit arrival of both warps has landed before TMEM is freed
+      mma_commit_elect(bar_done);
+      drain_all(W, bar_done, 0);
+    }
+    __syncwarp();
+  } else if (!L::SEP_P && warp == MMA_WARP0) {
+    // ------------------------------------------------------------ MMA issuer, both query tiles (whole warp, one lane issues)
     {
       constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);   // S = Q K^T: both K-major
       constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, L::ON, 1);  // O += P V: V is MN-major
       // Descriptor halves: the address field (low 14 bits, in 16-byte units) is the
       // only part that changes, and every offset added below stays inside it.
       const uint64_t dqk = make_sdesc_sw128(sbase, 16, 1024);        // K-major tiles (Q, K)
-      // MN-major V tiles; at d = 64 the leading-byte offset of stage 0 reaches the ones block
-      const uint64_t dvv = make_sdesc_sw128(sbase, L::LR_IN_TMEM ? L::ONES_OFF - L::KV_OFF : BOX_BYTES, 1024);
+      const uint64_t dvv = make_sdesc_sw128(sbase, BOX_BYTES, 1024);  // MN-major V tiles
       const uint32_t dqk_lo = uint32_t(dqk), dqk_hi = uint32_t(dqk >> 32);
       const uint32_t dv_lo = uint32_t(dvv), dv_hi = uint32_t(dvv >> 32);
       int stage = 0;
@@ -354,9 +515,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #define FA_ISSUE_PV(i, vs, acc)                                                                           \
   {                                                                                                       \
     const uint32_t s16 = ((vs) * L::TILE_BYTES) >> 4;                                                     \
-    const uint32_t b0 = dv_lo + (L::KV_OFF >> 4) + s16 - (L::LR_IN_TMEM ? (s16 << 16) : 0u);            \
+    const uint32_t b0 = dv_lo + (L::KV_OFF >> 4) + s16;                                                   \
     _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                                \
-      mma_ts_elect(tmem + L::o_col(i), tmem + L::s_col(i) + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi,        \
+      mma_ts_elect(tmem + L::o_col(i), tmem + L::p_col(i) + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi,        \
                   IDESC_PV, ((acc) || kk > 0) ? 1u : 0u);                                                 \
   }
 #define FA_TAKE(slot)                                                  \
@@ -434,7 +595,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       drain_all(W, bar_done, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
     const int i = warp / 4;         // query tile of this warpgroup
     const int wq = warp % 4;        // TMEM lane quarter this warp may access
@@ -442,7 +603,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_off + L::s_col(i);
     const uint32_t t_o = tmem + lane_off + L::o_col(i);
-    const uint32_t my_s_full = bar_s_full + 8 * i, my_p_full = bar_p_full + 8 * i;
+    const uint32_t t_p = tmem + lane_off + L::p_col(i);
+    const uint32_t my_s_full = bar_s_full + 8 * i, my_p_full = bar_p_full + 8 * i, my_s_free = bar_s_free + 8 * i;
     const uint32_t my_o_full = bar_o_full + 8 * i, my_o_empty = bar_o_empty + 8 * i;
     const float sl2 = p.scale_log2;
     uint32_t sf_phase = 0, of_phase = 0;
@@ -464,6 +626,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tc_fence_after();
         uint32_t sr[BN];
         tmem_ld128_wait(t_s, sr);
+        if (L::SEP_P) {  // S_i may now be overwritten by S_i(j+1)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(my_s_free);
+        }
         const int k0 = (u.jb + j) * BN;
         if ((p.causal && k0 + BN - 1 > q0) || k0 + BN > p.T) {  // diagonal or ragged tail tile
           int lim = p.T - k0;
@@ -501,9 +668,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const float nm = -m_run;
         float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;  // fp32 weights, two packed chains
         float lr0 = 0.f, lr1 = 0.f;                         // bf16 weights
+        uint32_t pk[BN / 2];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float x0, x1;
@@ -514,14 +681,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               fadd2(lb0, lb1, p0, p1);
             else
               fadd2(la0, la1, p0, p1);
-            pk[e] = pack_bf16x2(p0, p1);
-            if (!L::LR_IN_TMEM) add_bf16x2_f32(pk[e], lr0, lr1);
+            pk[16 * c + e] = pack_bf16x2(p0, p1);
+            // sum of the bf16 weights (the two forms measure fastest at d = 64 and d = 128)
+            if (L::SEP_P)  // bf16 -> fp32 is a shift / mask of the packed word, then one packed add
+              fadd2(lr0, lr1, u2f(pk[16 * c + e] << 16), u2f(pk[16 * c + e] & 0xFFFF0000u));
+            else
+              add_bf16x2_f32(pk[16 * c + e], lr0, lr1);
           }
-          tmem_st16(t_s + c * 16, pk);
+          if (!L::SEP_P) tmem_st16(t_p + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
+        }
+        if (L::SEP_P) {  // P_i(j-1) V_(j-1) must be done before P_i is overwritten and before O_i is rescaled
+          if (j > 0) {
+            if (!(ok = W.wait(my_o_full, of_phase))) break;
+            of_phase ^= 1;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_st16(t_p + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
         }
         l += (la0 + la1) + (lb0 + lb1);
         lr += lr0 + lr1;
-        if (rescale) {  // o *= r; PV_i(j-1) has completed (it was issued before S_i(j))
+        if (rescale) {  // o *= r; PV_i(j-1) has completed (it was issued before S_i(j), or waited for above)
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
@@ -530,7 +710,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (int e = 0; e < 32; ++e) ov[e] = f2u(u2f(ov[e]) * r);
             tmem_st32(t_o + c * 32, ov);
           }
-          if (L::LR_IN_TMEM) tmem_st1(t_o + D, f2u(u2f(tmem_ld1_wait(t_o + D)) * r));
         }
         tmem_wait_st();
         tc_fence_before();
@@ -542,7 +721,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (!(ok = W.wait(my_o_full, of_phase))) break;
       of_phase ^= 1;
       tc_fence_after();
-      if (L::LR_IN_TMEM) lr = u2f(tmem_ld1_wait(t_o + D));  // sum p~ formed by the P V MMA
       const float inv_l = 1.f / lr;
       if (PARTIAL) {  // this split's normalised output (fp32) and its LSE
         const int s = u.jb / p.split_tiles;
@@ -586,7 +764,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   tc_fence_before();
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == MMA_WARP0) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -625,7 +803,7 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(Layout<D>::THREADS);
   cfg.dynamicSmemBytes = Layout<D>::SMEM_BYTES;
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL>, q, k, v, p);
@@ -734,7 +912,7 @@ cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t str
 }
 
 int fa_fwd_smem_bytes(int d) { return d == 64 ? Layout<64>::SMEM_BYTES : Layout<128>::SMEM_BYTES; }
-int fa_fwd_threads() { return NUM_THREADS; }
+int fa_fwd_threads(int d) { return d == 64 ? Layout<64>::THREADS : Layout<128>::THREADS; }
 int fa_fwd_rows_per_unit() { return 2 * BM; }
 
 cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* out) {

@@ -9,7 +9,9 @@ namespace fa {
 struct Params {
   __nv_bfloat16* o;           // (B*H, T, d) bf16 output
   float* lse;                 // (B*H, T) fp32 output
-  int BH;                     // batch * heads
+  int BH;                     // batch * query heads
+  int H;                      // query heads per batch entry
+  int group;                  // query heads per K/V head (1 = multi-head; H / H_kv with grouped K/V)
   int T;                      // sequence length
   int causal;                 // 0 or 1
   int nqb;                    // 256-row query blocks per head: ceil(T / 256)
@@ -32,7 +34,7 @@ cudaError_t launch_fa_fwd_partial(int d, const CUtensorMap& q, const CUtensorMap
                                   const Params& p, int grid, cudaStream_t stream);
 cudaError_t launch_split_combine(int d, const Params& p, int num_sms, cudaStream_t stream);
 int fa_fwd_smem_bytes(int d);
-int fa_fwd_threads();
+int fa_fwd_threads(int d);
 int fa_fwd_rows_per_unit();
 cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* out);
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t stream);

@@ -155,6 +155,33 @@ def make_qkv(B: int, H: int, T: int, d: int, seed: int = 0,
     return QKV(B, H, T, d, q, k, v)
 
 
+@dataclass
+class GroupedQKV:
+    """Seeded inputs with grouped K/V heads: q (B, H, T, d), k and v (B, Hkv, T, d), bf16 bits."""
+
+    B: int
+    H: int
+    Hkv: int
+    T: int
+    d: int
+    q_bits: np.ndarray
+    k_bits: np.ndarray
+    v_bits: np.ndarray
+
+    def f64(self, name: str) -> np.ndarray:
+        heads = self.H if name == "q" else self.Hkv
+        return bf16_bits_to_f64(getattr(self, name + "_bits")).reshape(self.B, heads, self.T, self.d)
+
+
+def make_grouped_qkv(B: int, H: int, Hkv: int, T: int, d: int, seed: int = 0,
+                     sigma_qk: float = 1.0, sigma_v: float = 1.0) -> GroupedQKV:
+    """Q ~ N(0, sigma_qk^2) with H heads; K ~ N(0, sigma_qk^2) and V ~ N(0, sigma_v^2) with Hkv heads."""
+    q = normal_bf16_bits(seed, TENSOR_IDS["q"], B * H * T * d, sigma_qk).reshape(B, H, T, d)
+    k = normal_bf16_bits(seed, TENSOR_IDS["k"], B * Hkv * T * d, sigma_qk).reshape(B, Hkv, T, d)
+    v = normal_bf16_bits(seed, TENSOR_IDS["v"], B * Hkv * T * d, sigma_v).reshape(B, Hkv, T, d)
+    return GroupedQKV(B, H, Hkv, T, d, q, k, v)
+
+
 # The attention workloads: shapes, masks and value distributions.
 WORKLOADS = {
     "tiny_causal_b1h4t256d64": dict(B=1, H=4, T=256, d=64, causal=True, sigma_qk=1.0),

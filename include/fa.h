@@ -81,6 +81,25 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  cudaStream_t stream);
 
 /*
+ * Attention forward with grouped keys and values: H query heads share Hkv K/V
+ * heads, query head h reading K/V head h / (H / Hkv) of the same batch entry
+ * ("FlashAttention and Fused Kernels: Attention Without the n x n Matrix",
+ * section "Step 4: decoding is a different problem": Llama 3.1 8B shares each
+ * K/V head among 4 query heads).  Per query head the result is exactly the
+ * attention fa_fwd computes with that head's K and V.
+ *   q, o   : (B, H, T, d) bf16, as for fa_fwd.
+ *   k, v   : (B, Hkv, T, d) bf16, contiguous, d fastest.
+ *   lse    : (B, H, T) fp32.
+ *   Hkv    : 1 <= Hkv <= H with H % Hkv == 0 (Hkv == H is fa_fwd).
+ *   the rest as for fa_fwd.
+ * Errors: as fa_fwd; FA_ERR_BAD_SHAPE also when Hkv does not divide H; the
+ * pointer range checks use the K/V size B * Hkv * T * d.
+ */
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Hkv, int T, int d, int causal, float scale,
+                     cudaStream_t stream);
+
+/*
  * Attention forward with the keys of every row split into ranges that run as
  * separate work units (Flash-Decoding: "FlashAttention and Fused Kernels:
  * Attention Without the n x n Matrix", section "Flash-Decoding: split the

@@ -110,6 +110,39 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
     return O, lse
 
 
+def attention_fwd_gqa(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
+                      scale: float, rows=None):
+    """Attention with grouped K/V heads ("FlashAttention and Fused Kernels",
+    section "Step 4: decoding is a different problem": Llama 3.1 8B lets every
+    K/V head serve 4 query heads).
+
+    q is (B, H, T, d); k and v are (B, Hkv, T, d) with H a multiple of Hkv.
+    Query head h attends with K/V head h // (H // Hkv): per query head this is
+    exactly ``attention_head`` on that head's keys and values.  Returns O
+    (B, H, R, d) and LSE (B, H, R) as ``attention_fwd`` does.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, T, d = q.shape
+    Hkv = k.shape[1]
+    if H % Hkv != 0:
+        raise ValueError("the number of query heads must be a multiple of the K/V heads")
+    R = T if rows is None else len(rows)
+    O = np.empty((B, H, R, v.shape[3]), dtype=np.float64)
+    lse = np.empty((B, H, R), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            g = kv_head(h, H, Hkv)
+            O[b, h], lse[b, h] = attention_head(q[b, h], k[b, g], v[b, g], causal, scale, rows)
+    return O, lse
+
+
+def kv_head(h: int, H: int, Hkv: int) -> int:
+    """The K/V head that query head ``h`` reads: consecutive groups of H / Hkv query heads share one."""
+    return h // (H // Hkv)
+
+
 def probabilities(q: np.ndarray, k: np.ndarray, causal: bool, scale: float) -> np.ndarray:
     """The full probability matrix P of one head (T x T).  Small inputs only."""
     S = scores(np.asarray(q, np.float64), np.asarray(k, np.float64), scale)

@@ -250,6 +250,34 @@ def pin_row_subset_matches_full():
         assert np.array_equal(O[:, :, rows], Os) and np.array_equal(lse[:, :, rows], lses)
 
 
+def pin_gqa_brute_force_tiny():
+    """Grouped K/V heads: every query head equals plain-Python attention with K/V head h // (H / Hkv)."""
+    rng = _rng(22)
+    B, H, Hkv, T, d = 2, 6, 2, 5, 3
+    q = rng.standard_normal((B, H, T, d)) * 1.5
+    k, v = (rng.standard_normal((B, Hkv, T, d)) * 1.5 for _ in range(2))
+    for causal in (False, True):
+        O, lse = A.attention_fwd_gqa(q, k, v, causal, 0.7)
+        for b in range(B):
+            for h in range(H):
+                g = h // 3  # heads 0-2 read K/V head 0, heads 3-5 read K/V head 1
+                for i in range(T):
+                    ref, ref_lse = _brute_row(list(q[b, h, i]), [list(r) for r in k[b, g]], [list(r) for r in v[b, g]],
+                                              0.7, i + 1 if causal else T)
+                    assert np.allclose(O[b, h, i], ref, rtol=0, atol=1e-13), (b, h, i, causal)
+                    assert abs(lse[b, h, i] - ref_lse) < 1e-13
+
+
+def pin_gqa_one_group_per_head_is_mha():
+    """With as many K/V heads as query heads the grouped form is the ordinary one."""
+    rng = _rng(23)
+    q, k, v = (rng.standard_normal((2, 3, 9, 4)) for _ in range(3))
+    for causal in (False, True):
+        O1, l1 = A.attention_fwd_gqa(q, k, v, causal, 0.4)
+        O2, l2 = A.attention_fwd(q, k, v, causal, 0.4)
+        assert np.array_equal(O1, O2) and np.array_equal(l1, l2)
+
+
 # ---------------------------------------------------------------- online recurrence (test-only)
 
 def pin_online_f2_two_blocks():
@@ -356,7 +384,7 @@ ATTENTION_PINS = [
     pin_zero_queries_average_values, pin_constant_values, pin_identity_values_give_probabilities,
     pin_score_shift_moves_lse_only, pin_single_key, pin_two_keys_logistic, pin_causal_row0_is_v0,
     pin_causal_ignores_future, pin_key_permutation_invariance, pin_large_scores_stay_finite,
-    pin_brute_force_tiny, pin_row_subset_matches_full,
+    pin_brute_force_tiny, pin_row_subset_matches_full, pin_gqa_brute_force_tiny, pin_gqa_one_group_per_head_is_mha,
 ]
 ONLINE_PINS = [
     pin_online_f2_two_blocks, pin_online_f4_block_sizes, pin_online_f5_max_change,

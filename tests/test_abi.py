@@ -86,9 +86,9 @@ def test_launch_shape(lib):
     assert fa.fa_fwd_launch_shape(1, 4, 256, 64, True, 152)[0] == 4       # 4 units of 256 rows
     assert fa.fa_fwd_launch_shape(8, 12, 1024, 64, True, 152)[0] == 152   # 384 units, capped at the SMs
     g, t, s = fa.fa_fwd_launch_shape(1, 32, 4096, 128, False, 152)
-    assert (g, t) == (152, 320) and 128 * 1024 < s <= 232_448
+    assert (g, t) == (152, 320) and 128 * 1024 < s <= 232_448   # d = 128: one MMA-issuing warp
     g, t, s = fa.fa_fwd_launch_shape(1, 1, 1, 64, False, 152)
-    assert g == 1 and s <= 232_448
+    assert (g, t) == (1, 384) and s <= 232_448   # d = 64: one MMA-issuing warp per query tile
     with pytest.raises(fa.FAError):
         fa.fa_fwd_launch_shape(1, 1, 128, 80, False, 152)
 

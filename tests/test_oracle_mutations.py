@@ -76,6 +76,9 @@ MUTATIONS = {
     # weighted values
     "values_transposed_probabilities": (A, "weighted_values", lambda P, v: P.T @ v),
     "values_drop_last_key": (A, "weighted_values", lambda P, v: P[:, :-1] @ v[:-1]),
+    # grouped K/V heads
+    "gqa_heads_interleaved": (A, "kv_head", lambda h, H, Hkv: h % Hkv),
+    "gqa_group_off_by_one": (A, "kv_head", lambda h, H, Hkv: min((h + 1) // (H // Hkv), Hkv - 1)),
     # LSE
     "lse_drops_max": (A, "log_sum_exp", lambda m, l: np.log(l)),
     "lse_base2": (A, "log_sum_exp", lambda m, l: m + np.log2(l)),
