@@ -42,6 +42,9 @@ SWEEP_DEFAULT = ["tiny_causal_b1h4t256d64", "gpt2m_b16h16t1024d64", "gpt2m_stres
                  "llama8b_causal_b1h32t4096d128", "llama8b_b1h32t4096d128", "long_causal_b1h32t32768d128"]
 # split-KV (fa_fwd_splitkv) entries of the sweep: workload -> key splits
 SPLITKV_SWEEP = {"tiny_causal_b1h4t256d64": 2, "gpt2s_causal_b8h12t1024d64": 2, "llama8b_b1h32t4096d128": 2}
+# grouped K/V heads: Llama-3.1-8B attention (32 query heads sharing 8 K/V heads), causal and not
+GQA_SWEEP = {"llama8b_gqa_causal_b1h32kv8t4096d128": dict(B=1, H=32, Hkv=8, T=4096, d=128, causal=True),
+             "llama8b_gqa_b1h32kv8t4096d128": dict(B=1, H=32, Hkv=8, T=4096, d=128, causal=False)}
 
 
 def metric_flops(B, H, T, d, causal):
@@ -336,9 +339,46 @@ def time_splitkv(fa, torch, dev, w, qkv, scale, num_splits, steps):
     return sum(ms) / len(ms) / 1e3, ws.numel()
 
 
-def run_sweep(fa, torch, dev, names, peaks, splitkv=SPLITKV_SWEEP):
+def time_gqa(fa, torch, dev, g, steps):
+    """Device time of fa_fwd_gqa per step (inputs rotating past L2)."""
+    B, H, Hkv, T, d, causal = g["B"], g["H"], g["Hkv"], g["T"], g["d"], g["causal"]
+    x = fi.make_grouped_qkv(B, H, Hkv, T, d, seed=0)
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q0, k0, v0 = up(x.q_bits), up(x.k_bits), up(x.v_bits)
+    set_bytes = (2 * q0.numel() + 2 * k0.numel()) * 2
+    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
+    sets = [(q0, k0, v0) if s == 0 else (q0.clone(), k0.clone(), v0.clone()) for s in range(nsets)]
+    sets = [(q, k, v, torch.empty_like(q), torch.empty((B, H, T), dtype=torch.float32, device=dev))
+            for q, k, v in sets]
+    stream = torch.cuda.current_stream(dev)
+    scale = 1.0 / math.sqrt(d)
+    for i in range(5):
+        fa.fa_fwd_gqa(*sets[i % nsets], causal, scale, stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fa.fa_fwd_gqa(*sets[i % nsets], causal, scale, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return sum(ms) / len(ms) / 1e3
+
+
+def run_sweep(fa, torch, dev, names, peaks, splitkv=SPLITKV_SWEEP, gqa=GQA_SWEEP):
     """Every other workload, measured the same way with fewer steps (informational)."""
     out = {}
+    for name, g in gqa.items():
+        f = metric_flops(g["B"], g["H"], g["T"], g["d"], g["causal"])
+        steps = int(min(2000, max(20, 0.5 / max(f / 1.0e15, 1e-6))))
+        sec = time_gqa(fa, torch, dev, g, steps)
+        out[name] = {"ms_mean": round(sec * 1e3, 4), "tflops": round(f / sec / 1e12, 1),
+                     "pct_of_bf16_peak": round(100 * f / sec / 1e12 / peaks["bf16_tflops"], 1),
+                     "steps": steps, "kernels": "fa_fwd_kernel (grouped K/V heads)"}
+        torch.cuda.empty_cache()
     for name, ns in splitkv.items():
         w = fi.WORKLOADS[name]
         qkv = fi.make_qkv(w["B"], w["H"], w["T"], w["d"], seed=0, sigma_qk=w["sigma_qk"])

@@ -16,6 +16,7 @@ import os
 import numpy as np
 
 import oracle.attention as A
+import oracle.backward as BW
 import oracle.online as ON
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
@@ -379,6 +380,72 @@ def pin_split_combine_matches_oracle():
             assert np.allclose(y2, O[0, 0, i], atol=1e-13) and abs(l2 - lse[0, 0, i]) < 1e-12
 
 
+# ---------------------------------------------------------------- backward pass
+
+def _loss(q, k, v, do, causal, scale):
+    """sum(dO * O) with O from the forward oracle: its gradient is what the backward pass returns."""
+    O, _ = A.attention_fwd(q[None, None], k[None, None], v[None, None], causal, scale)
+    return float((do * O[0, 0]).sum())
+
+
+def pin_bwd_finite_differences():
+    """Central differences of sum(dO * O) through the forward oracle agree with the backward oracle."""
+    rng = _rng(30)
+    h = 1e-6
+    for T, d, causal, scale in ((4, 3, False, 0.7), (5, 2, True, 1.1), (3, 4, True, 0.4)):
+        q, k, v, do = (rng.standard_normal((T, d)) for _ in range(4))
+        dq, dk, dv = BW.attention_bwd(q[None, None], k[None, None], v[None, None], do[None, None], causal, scale)
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = {"q": q, "k": k, "v": v}
+                args_m = dict(args_p)
+                args_p[name], args_m[name] = xp, xm
+                num[idx] = (_loss(args_p["q"], args_p["k"], args_p["v"], do, causal, scale)
+                            - _loss(args_m["q"], args_m["k"], args_m["v"], do, causal, scale)) / (2 * h)
+            assert np.allclose(g[0, 0], num, rtol=0, atol=2e-8), (name, T, causal, np.abs(g[0, 0] - num).max())
+
+
+def pin_bwd_constant_values():
+    """If every value row is the same, O does not depend on Q or K: dQ = dK = 0 and dV = P^T dO."""
+    rng = _rng(31)
+    T, d = 6, 4
+    q, k, do = (rng.standard_normal((T, d)) for _ in range(3))
+    v = np.tile(rng.standard_normal(d), (T, 1))
+    for causal in (False, True):
+        dq, dk, dv = BW.attention_bwd(q[None, None], k[None, None], v[None, None], do[None, None], causal, 0.5)
+        assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
+        P = A.probabilities(q, k, causal, 0.5)
+        assert np.allclose(dv[0, 0], P.T @ do, atol=1e-14)
+
+
+def pin_bwd_sums():
+    """Each row of P sums to 1, so the dV rows sum to the dO rows; a common shift of every key
+    leaves the softmax unchanged, so the dK rows sum to zero."""
+    rng = _rng(32)
+    q, k, v, do = (rng.standard_normal((2, 3, 11, 5)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = BW.attention_bwd(q, k, v, do, causal, 0.3)
+        assert np.allclose(dv.sum(axis=2), do.sum(axis=2), atol=1e-12)
+        assert np.abs(dk.sum(axis=2)).max() < 1e-12
+
+
+def pin_bwd_row_dot():
+    """sum_k P_ik dP_ik equals sum_c dO_ic O_ic."""
+    rng = _rng(33)
+    T, d = 9, 4
+    q, k, v, do = (rng.standard_normal((T, d)) for _ in range(4))
+    P = BW.probabilities_head(q, k, True, 0.6)
+    dP = BW.grad_probabilities(do, v)
+    assert np.allclose((P * dP).sum(axis=1), BW.row_dot(do, P @ v), atol=1e-13)
+
+
+BACKWARD_PINS = [pin_bwd_finite_differences, pin_bwd_constant_values, pin_bwd_sums, pin_bwd_row_dot]
+
+
 ATTENTION_PINS = [
     pin_f1_three_token_causal, pin_f2_four_scores, pin_f4_lesson_fixture,
     pin_zero_queries_average_values, pin_constant_values, pin_identity_values_give_probabilities,
@@ -391,4 +458,4 @@ ONLINE_PINS = [
     pin_online_f1_row2_two_tiles, pin_online_equals_three_step, pin_split_combine_f3,
     pin_split_combine_matches_oracle,
 ]
-ALL_PINS = ATTENTION_PINS + ONLINE_PINS
+ALL_PINS = ATTENTION_PINS + ONLINE_PINS + BACKWARD_PINS

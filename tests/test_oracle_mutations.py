@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import oracle.attention as A
+import oracle.backward as BW
 import oracle.online as ON
 from oracle_pins import ALL_PINS
 
@@ -79,6 +80,15 @@ MUTATIONS = {
     # grouped K/V heads
     "gqa_heads_interleaved": (A, "kv_head", lambda h, H, Hkv: h % Hkv),
     "gqa_group_off_by_one": (A, "kv_head", lambda h, H, Hkv: min((h + 1) // (H // Hkv), Hkv - 1)),
+    # backward pass
+    "bwd_dv_untransposed": (BW, "grad_values", lambda P, do: P @ do),
+    "bwd_dp_rescaled": (BW, "grad_probabilities", lambda do, v: (do @ v.T) * 1.0001),
+    "bwd_ds_drops_row_dot": (BW, "grad_scores", lambda P, dP, D: P * dP),
+    "bwd_ds_row_dot_sign": (BW, "grad_scores", lambda P, dP, D: P * (dP + D[:, None])),
+    "bwd_dq_no_scale": (BW, "grad_queries", lambda dS, k, s: dS @ k),
+    "bwd_dq_transposed": (BW, "grad_queries", lambda dS, k, s: s * (dS.T @ k)),
+    "bwd_dk_untransposed": (BW, "grad_keys", lambda dS, q, s: s * (dS @ q)),
+    "bwd_row_dot_squared": (BW, "row_dot", lambda do, o: (do * o * o).sum(axis=1)),
     # LSE
     "lse_drops_max": (A, "log_sum_exp", lambda m, l: np.log(l)),
     "lse_base2": (A, "log_sum_exp", lambda m, l: m + np.log2(l)),
