@@ -39,7 +39,7 @@ STATUS = {
     11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA", 13: "FA_ERR_WORKSPACE",
 }
 FA_MAX_SPLITS = 256
-EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
+EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
             "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version"]
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -70,6 +70,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd.restype = i
     lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa_fwd_gqa.restype = i
+    lib.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -190,6 +194,46 @@ def attention_gqa(q, k, v, causal: bool = False, scale: float | None = None, str
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     fa_fwd_gqa(q, k, v, o, lse, causal, scale, stream)
     return o, lse
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, T: int) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(B, H, T))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> None:
+    """dQ, dK, dV of sum(dO * O) into caller-owned bf16 tensors (all (B, H, T, d), contiguous).
+
+    ``o`` and ``lse`` are what ``fa_fwd`` returned for (q, k, v, causal, scale);
+    ``workspace`` is a CUDA tensor of at least ``fa_bwd_workspace_bytes(B, H, T)`` bytes.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    B, H, T, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 (B, H, T) tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    code = load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, T, d,
+                                 int(bool(causal)), float(scale), workspace.data_ptr(), nbytes,
+                                 ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_bwd")
+
+
+def attention_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocates dQ, dK, dV and the workspace and runs ``fa_bwd``; ``scale`` defaults to 1/sqrt(d)."""
+    import torch
+
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa_bwd_workspace_bytes(B, H, T), dtype=torch.uint8, device=q.device)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale, ws, stream)
+    return dq, dk, dv
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):

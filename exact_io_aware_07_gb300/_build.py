@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libfa_gb300.so"
 
-SOURCES = ["fa_kernel.cu", "fa_api.cu"]
+SOURCES = ["fa_kernel.cu", "fa_bwd.cu", "fa_api.cu"]
 HEADERS = ["fa_kernel.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

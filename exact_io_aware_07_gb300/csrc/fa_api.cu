@@ -309,6 +309,74 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   return launch_splitkv(pr, d, num_splits, static_cast<float*>(workspace), stream);
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int T) {
+  if (B < 1 || H < 1 || T < 1) return 0;
+  const size_t bytes = static_cast<size_t>(B) * H * T * 4;
+  return (bytes + 255) / 256 * 256;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int H, int T, int d, int causal, float scale, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
+  fa_status st = validate_host(q, k, v, o, lse, B, H, T, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (!dout || !dq || !dk || !dv) return FA_ERR_NULL_PTR;
+  for (const void* x : {dout, static_cast<const void*>(dq), static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return FA_ERR_MISALIGNED;
+  const size_t need = fa_bwd_workspace_bytes(B, H, T);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return FA_ERR_MISALIGNED;
+  int dev = 0, num_sms = 0;
+  if ((st = current_device(&dev, &num_sms)) != FA_OK) return st;
+  const int BH = B * H;
+  const size_t t_bytes = static_cast<size_t>(BH) * T * d * 2, r_bytes = static_cast<size_t>(BH) * T * 4;
+  const struct {
+    const void* p;
+    size_t n;
+  } ins[6] = {{q, t_bytes}, {k, t_bytes}, {v, t_bytes}, {o, t_bytes}, {dout, t_bytes}, {lse, r_bytes}},
+    outs[4] = {{dq, t_bytes}, {dk, t_bytes}, {dv, t_bytes}, {workspace, need}};
+  for (const auto& x : ins)
+    if ((st = check_device_range(x.p, x.n, dev)) != FA_OK) return st;
+  for (const auto& x : outs)
+    if ((st = check_device_range(x.p, x.n, dev)) != FA_OK) return st;
+  for (int a = 0; a < 4; ++a) {
+    for (const auto& x : ins)
+      if (overlaps(outs[a].p, outs[a].n, x.p, x.n)) return FA_ERR_ALIAS;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a].p, outs[a].n, outs[b].p, outs[b].n)) return FA_ERR_ALIAS;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tensor_map(&tq, q, BH, T, d) || !make_tensor_map(&tk, k, BH, T, d) ||
+      !make_tensor_map(&tv, v, BH, T, d) || !make_tensor_map(&tdo, dout, BH, T, d))
+    return FA_ERR_CUDA;
+  fa::BwdParams p{};
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.drow = static_cast<float*>(workspace);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.BH = BH;
+  p.T = T;
+  p.causal = causal;
+  p.nt = (T + 127) / 128;
+  const long long units = static_cast<long long>(BH) * p.nt;
+  if (units > INT_MAX) return FA_ERR_BAD_SHAPE;
+  p.num_units = static_cast<int>(units);
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.timeout_ns = kWaitLimitNs;
+  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
+  if (fa::launch_bwd_rowdot(d, p, num_sms, stream) != cudaSuccess ||
+      fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid, stream) != cudaSuccess ||
+      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
 static_assert(FA_NOALLOC_SCRATCH_BYTES == fa::kNoAllocScratchBytes, "fa.h and the kernel disagree on the scratch size");
 
 const char* fa_status_string(fa_status s) {
@@ -326,18 +394,20 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_BAD_POINTER: return "a pointer is not device memory of the current device, or its allocation is too small";
     case FA_ERR_ALIAS: return "an output overlaps an input or the other output";
     case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
-    case FA_ERR_WORKSPACE: return "the split-KV workspace is missing or smaller than fa_fwd_splitkv_workspace_bytes()";
+    case FA_ERR_WORKSPACE: return "the workspace is missing or smaller than the size its *_workspace_bytes() gives";
   }
   return "unknown status";
 }
 
 fa_status fa_device_status(cudaStream_t stream, int* out) {
   if (!out) return FA_ERR_NULL_PTR;
-  unsigned int word = 0;
-  if (fa::read_and_clear_status(stream, &word) != cudaSuccess) {
+  unsigned int word = 0, bwd = 0;
+  if (fa::read_and_clear_status(stream, &word) != cudaSuccess ||
+      fa::read_and_clear_bwd_status(stream, &bwd) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }
+  word |= bwd;
   *out = word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
   return FA_OK;
 }

@@ -1,0 +1,591 @@
+// FlashAttention backward for sm_103a: the gradients of sum(dO * O) with
+// respect to Q, K and V, recomputing S and P from the stored log-sum-exp
+// ("FlashAttention and Fused Kernels: Attention Without the n x n Matrix",
+// section "Training: recompute instead of store"; "Flash Attention, tiled",
+// section "More arithmetic can still be faster").  With P = exp(S - LSE) and
+// D_t = sum_c dO_tc O_tc:
+//   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q.
+//
+// Three kernels, no atomics and no T x T matrix in memory:
+//   fa_bwd_rowdot_kernel  D for every row (one warp per row);
+//   fa_bwd_dq_kernel      per (head, 128-row query tile): stream the key tiles,
+//                         S = Q K^T and dP = dO V^T on the tensor core, dS in the
+//                         softmax warps, dQ += dS K (dS read from Tensor Memory);
+//   fa_bwd_dkdv_kernel    per (head, 128-key tile): stream the query tiles,
+//                         S^T = K Q^T and dP^T = V dO^T, P^T and dS^T in the
+//                         softmax warps, dV += P^T dO and dK += dS^T Q (P^T and
+//                         dS^T read from Tensor Memory).
+// Each recomputes S and dP (seven matrix products per tile pair instead of
+// five) so that every product takes its A operand from Tensor Memory with the
+// rows it needs on the lanes, and no partial sum crosses CTAs.
+//
+// Roles (192 threads, one CTA per SM, persistent over work units):
+//   warps 0-3  one TMEM lane (one row of the unit's 128-row tile) per thread
+//   warp 4     TMA producer: the unit's two resident tiles, then the streamed
+//              tiles through a ring
+//   warp 5     Tensor Memory allocator and tcgen05.mma issuer (whole warp,
+//              elect.sync picks the issuing lane)
+// Every mbarrier wait is bounded; on expiry the kernel records it in its
+// status word and unwinds, as the forward kernel does.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_kernel.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BT = 128;  // rows per tile (queries or keys)
+constexpr int BWD_THREADS = 192;
+constexpr int BWD_PRODUCER = 4;
+constexpr int BWD_MMA = 5;
+constexpr int BOX = 128 * 128;  // one TMA box: 128 rows x 64 bf16, 128-byte swizzle
+constexpr float LOG2E = 1.4426950408889634074f;
+
+__device__ unsigned int g_bwd_status;  // bit 0: a bounded wait ran out
+
+template <int D>
+struct BwdLayout {
+  static constexpr int TILE = BT * D * 2;
+  static constexpr int BOXES = D / 64;
+  static constexpr int STAGES = (D == 128) ? 4 : 6;  // streamed tiles in flight
+  static constexpr int RES_OFF = 0;                  // two resident tiles
+  static constexpr int RING_OFF = 2 * TILE;
+  static constexpr int VEC_OFF = RING_OFF + STAGES * TILE;  // [2 buffers][LSE*log2e, D][128] fp32
+  static constexpr int BAR_OFF = VEC_OFF + 2 * 2 * BT * 4;
+  // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2]
+  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;
+};
+static_assert(BwdLayout<128>::SMEM <= 232448 && BwdLayout<64>::SMEM <= 232448, "shared memory over the limit");
+
+// Tensor Memory columns (512 allocated):
+//   dQ kernel:    S [0,128)    dP [128,256)    dQ [256,256+d)
+//   dK/dV kernel: S^T [0,128)  dP^T [128,256)  dV [256,256+d)  dK [256+d,256+2d)
+// P / dS (bf16 pairs) are written over the first 64 columns of S / dP.
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256;
+
+struct Bars {
+  uint32_t res_full, res_empty, ring_full, ring_empty, s_full, p_full, o_full, o_empty, done;
+  uint32_t vec_full;  // [2]: the per-step LSE / D vectors of the dK/dV kernel are in shared memory
+};
+
+template <int D>
+__device__ __forceinline__ Bars make_bars(uint32_t base) {
+  using L = BwdLayout<D>;
+  Bars b;
+  b.res_full = base;
+  b.res_empty = base + 8;
+  b.ring_full = base + 16;
+  b.ring_empty = base + 16 + 8 * L::STAGES;
+  const uint32_t x = base + 16 + 16 * L::STAGES;
+  b.s_full = x;
+  b.p_full = x + 8;
+  b.o_full = x + 16;
+  b.o_empty = x + 24;
+  b.done = x + 32;
+  b.vec_full = x + 40;
+  return b;
+}
+
+// The k-th unit of CTA b in a grid of G (snake over a heavy-first list).
+__device__ __forceinline__ int bwd_unit_of(int k, int b, int G) { return k * G + ((k & 1) ? (G - 1 - b) : b); }
+
+// ---------------------------------------------------------------- D = rowsum(dO * O)
+
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
+  constexpr int CPL = D / 32;
+  const int lane = threadIdx.x % 32;
+  const size_t rows = static_cast<size_t>(p.BH) * p.T;
+  const size_t warps = gridDim.x * (blockDim.x / 32);
+  for (size_t r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < rows; r += warps) {
+    const __nv_bfloat16* o = p.o + r * D + lane * CPL;
+    const __nv_bfloat16* g = p.dout + r * D + lane * CPL;
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; c += 2) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + c));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(g + c));
+      acc = fmaf(a.x, b.x, acc);
+      acc = fmaf(a.y, b.y, acc);
+    }
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) p.drow[r] = acc;
+  }
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+// Common prologue: barriers, Tensor Memory, abort flag.  Returns the TMEM base.
+template <int D>
+__device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint32_t* tmem_slot,
+                                              volatile int* abort_flag, int warp) {
+  using L = BwdLayout<D>;
+  if (threadIdx.x == 0) {
+    mbar_init(B.res_full, 1);
+    mbar_init(B.res_empty, 1);
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(B.ring_full + 8 * s, 1);
+      mbar_init(B.ring_empty + 8 * s, 1);
+    }
+    mbar_init(B.s_full, 1);
+    mbar_init(B.p_full, 4);
+    mbar_init(B.o_full, 1);
+    mbar_init(B.o_empty, 4);
+    mbar_init(B.done, 1);
+    mbar_init(B.vec_full, 128);
+    mbar_init(B.vec_full + 8, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == BWD_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return *tmem_slot;
+}
+
+template <int D>
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == BWD_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Unit w -> (head, resident tile, first streamed tile, number of streamed tiles).
+// KIND 0 (dQ): resident = the query tile (Q, dO), streamed = key tiles (K, V);
+//   causal units are listed longest first (query tile nt-1 first).
+// KIND 1 (dK, dV): resident = the key tile (K, V), streamed = query tiles (Q, dO);
+//   causal units are listed longest first (key tile 0 first).
+template <int KIND>
+__device__ __forceinline__ void bwd_decode(const BwdParams& p, int w, int& bh, int& rt, int& first, int& n) {
+  const int band = w / p.BH;
+  bh = w - band * p.BH;
+  if (KIND == 0) {
+    rt = p.causal ? p.nt - 1 - band : band;
+    first = 0;
+    n = p.causal ? rt + 1 : p.nt;
+  } else {
+    rt = band;
+    first = p.causal ? rt : 0;
+    n = p.nt - first;
+  }
+}
+
+// TMA producer (whole warp, one lane issues).  Per unit: the two resident tiles
+// from (mapA, mapB) at tile rt, then the streamed tiles from (mapC, mapD) at tiles
+// first .. first+n-1 in the order C_0 D_0 C_1 D_1 ...
+template <int D, int KIND>
+__device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t sbase,
+                                             const CUtensorMap* mapA, const CUtensorMap* mapB,
+                                             const CUtensorMap* mapC, const CUtensorMap* mapD) {
+  using L = BwdLayout<D>;
+  const int lane = threadIdx.x % 32;
+  if (lane == 0) {
+    tma_prefetch_desc(mapA);
+    tma_prefetch_desc(mapB);
+    tma_prefetch_desc(mapC);
+    tma_prefetch_desc(mapD);
+  }
+  const int G = gridDim.x;
+  int stage = 0, nu = 0;
+  uint32_t phase = 0, issued = 0, issued_parity = 0;
+  bool res_issued = false, ok = true;
+  uint32_t res_parity = 0;
+  for (int k = 0; ok && k * G < p.num_units; ++k) {
+    const int w = bwd_unit_of(k, blockIdx.x, G);
+    if (w >= p.num_units) continue;
+    int bh, rt, first, n;
+    bwd_decode<KIND>(p, w, bh, rt, first, n);
+    if (!(ok = wait_all(W, B.res_empty, (nu & 1) ^ 1))) break;
+    mbar_arrive_expect_tx_elect(B.res_full, 2 * L::TILE);
+#pragma unroll
+    for (int b = 0; b < L::BOXES; ++b) {
+      tma_load_3d_elect(sbase + L::RES_OFF + b * BOX, mapA, b * 64, rt * BT, bh, B.res_full);
+      tma_load_3d_elect(sbase + L::RES_OFF + L::TILE + b * BOX, mapB, b * 64, rt * BT, bh, B.res_full);
+    }
+    res_issued = true;
+    res_parity = nu & 1;
+    ++nu;
+    for (int t = 0; ok && t < 2 * n; ++t) {
+      if (!(ok = wait_all(W, B.ring_empty + 8 * stage, phase ^ 1))) break;
+      mbar_arrive_expect_tx_elect(B.ring_full + 8 * stage, L::TILE);
+#pragma unroll
+      for (int b = 0; b < L::BOXES; ++b)
+        tma_load_3d_elect(sbase + L::RING_OFF + stage * L::TILE + b * BOX, (t & 1) ? mapD : mapC, b * 64,
+                          (first + (t >> 1)) * BT, bh, B.ring_full + 8 * stage);
+      issued |= 1u << stage;
+      issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == L::STAGES) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+  }
+  if (!ok) {  // let every copy already issued land before the CTA exits
+    if (res_issued) drain_all(W, B.res_full, res_parity);
+    for (int s = 0; s < L::STAGES; ++s)
+      if (issued & (1u << s)) drain_all(W, B.ring_full + 8 * s, (issued_parity >> s) & 1u);
+  }
+}
+
+// MMA issuer (whole warp, one lane issues).
+//   KIND 0: S = Q K^T, dP = dO V^T; after the softmax warps wrote dS: dQ += dS K.
+//   KIND 1: S^T = K Q^T, dP^T = V dO^T; after P^T, dS^T: dV += P^T dO, dK += dS^T Q.
+template <int D, int KIND>
+__device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t sbase,
+                                        uint32_t tmem) {
+  using L = BwdLayout<D>;
+  constexpr uint32_t IDESC_S = make_idesc_bf16(BT, BT, 0);  // both operands K-major (d contiguous)
+  constexpr uint32_t IDESC_G = make_idesc_bf16(BT, D, 1);   // B MN-major: rows of d contiguous elements
+  const uint64_t dk = make_sdesc_sw128(sbase, 16, 1024);
+  const uint64_t dm = make_sdesc_sw128(sbase, BOX, 1024);  // the second 64-column chunk is one box further
+  const uint32_t dk_lo = uint32_t(dk), dk_hi = uint32_t(dk >> 32);
+  const uint32_t dm_lo = uint32_t(dm), dm_hi = uint32_t(dm >> 32);
+  const int G = gridDim.x;
+  int stage = 0, nu = 0;
+  uint32_t phase = 0, pf = 0, oe = 0;
+  bool ok = true;
+  for (int k = 0; ok && k * G < p.num_units; ++k) {
+    const int w = bwd_unit_of(k, blockIdx.x, G);
+    if (w >= p.num_units) continue;
+    int bh, rt, first, n;
+    bwd_decode<KIND>(p, w, bh, rt, first, n);
+    if (!(ok = wait_all(W, B.res_full, nu & 1))) break;
+    ++nu;
+    tc_fence_after();
+#define BWD_TAKE(slot)                                                   \
+  {                                                                      \
+    slot = stage;                                                        \
+    if (!(ok = wait_all(W, B.ring_full + 8 * stage, phase))) break;      \
+    if (++stage == L::STAGES) {                                          \
+      stage = 0;                                                         \
+      phase ^= 1;                                                        \
+    }                                                                    \
+    tc_fence_after();                                                    \
+  }
+    for (int t = 0; t < n; ++t) {
+      int s0 = 0, s1 = 0;  // ring stages of this step's two streamed tiles
+      BWD_TAKE(s0);
+      BWD_TAKE(s1);
+      // the two score-like products: [resident tile 0] x [streamed tile 0]^T, [resident 1] x [streamed 1]^T
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk / 4) * BOX + (kk % 4) * 32) >> 4;
+        mma_ss_elect(tmem + COL_S, dk_lo + (L::RES_OFF >> 4) + off, dk_hi,
+                     dk_lo + ((L::RING_OFF + s0 * L::TILE) >> 4) + off, dk_hi, IDESC_S, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk / 4) * BOX + (kk % 4) * 32) >> 4;
+        mma_ss_elect(tmem + COL_DP, dk_lo + ((L::RES_OFF + L::TILE) >> 4) + off, dk_hi,
+                     dk_lo + ((L::RING_OFF + s1 * L::TILE) >> 4) + off, dk_hi, IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(B.s_full);
+      if (t == 0) {
+        if (!(ok = wait_all(W, B.o_empty, oe ^ 1))) break;
+        oe ^= 1;
+      }
+      if (!(ok = wait_all(W, B.p_full, pf))) break;
+      pf ^= 1;
+      tc_fence_after();
+      const uint32_t acc0 = t > 0 ? 1u : 0u;
+      if (KIND == 0) {
+        // dQ += dS K_j: A = dS (bf16 pairs over S), B = K_j (streamed tile 0) MN-major
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+          mma_ts_elect(tmem + COL_ACC, tmem + COL_S + kk * 8,
+                       dm_lo + ((L::RING_OFF + s0 * L::TILE + kk * 2048) >> 4), dm_hi, IDESC_G, acc0 | (kk > 0));
+      } else {
+        // dV += P^T dO_i (B = streamed tile 1), dK += dS^T Q_i (B = streamed tile 0)
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+          mma_ts_elect(tmem + COL_ACC, tmem + COL_S + kk * 8,
+                       dm_lo + ((L::RING_OFF + s1 * L::TILE + kk * 2048) >> 4), dm_hi, IDESC_G, acc0 | (kk > 0));
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+          mma_ts_elect(tmem + COL_ACC + D, tmem + COL_DP + kk * 8,
+                       dm_lo + ((L::RING_OFF + s0 * L::TILE + kk * 2048) >> 4), dm_hi, IDESC_G, acc0 | (kk > 0));
+      }
+      mma_commit_elect(B.ring_empty + 8 * s0);
+      mma_commit_elect(B.ring_empty + 8 * s1);
+      if (t + 1 == n) {
+        mma_commit_elect(B.res_empty);
+        mma_commit_elect(B.o_full);
+      }
+    }
+#undef BWD_TAKE
+  }
+  // every MMA and commit arrival has landed before Tensor Memory is freed
+  mma_commit_elect(B.done);
+  drain_all(W, B.done, 0);
+}
+
+// Softmax-side warps of the dQ kernel: thread = query row.  For each key tile:
+// P = exp(S - LSE) (masked entries 0), dS = P (dP - D) in bf16 over S; at the end
+// of the unit dQ = scale * (sum dS K) in bf16.
+template <int D>
+__device__ __forceinline__ void bwd_dq_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int r = warp * 32 + lane;
+  const uint32_t lane_off = uint32_t(warp * 32) << 16;
+  const uint32_t t_s = tmem + lane_off + COL_S, t_dp = tmem + lane_off + COL_DP, t_acc = tmem + lane_off + COL_ACC;
+  const float sl2 = p.scale_log2;
+  const int G = gridDim.x;
+  uint32_t sf = 0, of = 0;
+  bool ok = true;
+  for (int k = 0; ok && k * G < p.num_units; ++k) {
+    const int w = bwd_unit_of(k, blockIdx.x, G);
+    if (w >= p.num_units) continue;
+    int bh, rt, first, n;
+    bwd_decode<0>(p, w, bh, rt, first, n);
+    const int q0 = rt * BT, row = q0 + r;
+    const size_t ri = static_cast<size_t>(bh) * p.T + row;
+    const float lse2 = row < p.T ? p.lse[ri] * LOG2E : 0.f;
+    const float drow = row < p.T ? p.drow[ri] : 0.f;
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = W.wait(B.s_full, sf))) break;
+      sf ^= 1;
+      tc_fence_after();
+      const int k0 = j * BT;
+      // keys this row may use in the tile: all, or up to the diagonal / the end of the sequence
+      int lim = BT;
+      if ((p.causal && k0 + BT - 1 > q0) || k0 + BT > p.T) {
+        lim = p.T - k0;
+        if (p.causal) lim = min(lim, row - k0 + 1);
+      }
+#pragma unroll
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32x2_wait(t_s + 32 * c, sv, t_dp + 32 * c, dv);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = 32 * c + 2 * e;
+          float p0 = ex2_approx(fmaf(u2f(sv[2 * e]), sl2, -lse2));
+          float p1 = ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, -lse2));
+          if (c0 >= lim) p0 = 0.f;
+          if (c0 + 1 >= lim) p1 = 0.f;
+          pk[e] = pack_bf16x2(p0 * (u2f(dv[2 * e]) - drow), p1 * (u2f(dv[2 * e + 1]) - drow));
+        }
+        tmem_st16(t_s + 16 * c, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.p_full);
+    }
+    if (!ok) break;
+    if (!(ok = W.wait(B.o_full, of))) break;
+    of ^= 1;
+    tc_fence_after();
+    __nv_bfloat16* out = p.dq + ri * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32_wait(t_acc + 32 * c, v);
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * p.scale, u2f(v[2 * e + 1]) * p.scale);
+      if (row < p.T) {
+        uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.o_empty);
+  }
+}
+
+// Softmax-side warps of the dK/dV kernel: thread = key row.  For each query tile:
+// P^T = exp(S^T - LSE) and dS^T = P^T (dP^T - D) with the tile's LSE and D read
+// from shared memory (every lane reads the same word: a broadcast); P^T over S^T
+// and dS^T over dP^T in bf16.  At the end of the unit dV and dK = scale * (...) in bf16.
+template <int D>
+__device__ __forceinline__ void bwd_dkdv_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem,
+                                              float* vec) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int r = warp * 32 + lane;
+  const uint32_t lane_off = uint32_t(warp * 32) << 16;
+  const uint32_t t_s = tmem + lane_off + COL_S, t_dp = tmem + lane_off + COL_DP, t_acc = tmem + lane_off + COL_ACC;
+  const float sl2 = p.scale_log2;
+  const int G = gridDim.x;
+  uint32_t sf = 0, of = 0;
+  int it = 0;  // steps so far: picks the vector buffer and its barrier phase
+  bool ok = true;
+  for (int k = 0; ok && k * G < p.num_units; ++k) {
+    const int w = bwd_unit_of(k, blockIdx.x, G);
+    if (w >= p.num_units) continue;
+    int bh, rt, first, n;
+    bwd_decode<1>(p, w, bh, rt, first, n);
+    const int k0 = rt * BT, key = k0 + r;
+    for (int t = 0; t < n; ++t, ++it) {
+      const int q0 = (first + t) * BT;
+      float* lv = vec + (it & 1) * 2 * BT;  // [0, 128): LSE * log2 e; [128, 256): D
+      {
+        const int q = q0 + r;
+        const size_t qi = static_cast<size_t>(bh) * p.T + q;
+        lv[r] = q < p.T ? p.lse[qi] * LOG2E : INFINITY;  // rows past T: P = 0
+        lv[BT + r] = q < p.T ? p.drow[qi] : 0.f;
+        mbar_arrive(B.vec_full + 8 * (it & 1));
+      }
+      if (!(ok = W.wait(B.vec_full + 8 * (it & 1), (it >> 1) & 1))) break;
+      if (!(ok = W.wait(B.s_full, sf))) break;
+      sf ^= 1;
+      tc_fence_after();
+      const bool diag = p.causal && q0 == k0;  // query q sees this key only if q >= key
+#pragma unroll
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32x2_wait(t_s + 32 * c, sv, t_dp + 32 * c, dv);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = 32 * c + 2 * e;
+          const float2 l2 = *reinterpret_cast<const float2*>(lv + c0);
+          const float2 dd = *reinterpret_cast<const float2*>(lv + BT + c0);
+          float p0 = ex2_approx(fmaf(u2f(sv[2 * e]), sl2, -l2.x));
+          float p1 = ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, -l2.y));
+          if (diag && c0 < r) p0 = 0.f;
+          if (diag && c0 + 1 < r) p1 = 0.f;
+          pp[e] = pack_bf16x2(p0, p1);
+          pd[e] = pack_bf16x2(p0 * (u2f(dv[2 * e]) - dd.x), p1 * (u2f(dv[2 * e + 1]) - dd.y));
+        }
+        tmem_st16(t_s + 16 * c, pp);
+        tmem_st16(t_dp + 16 * c, pd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.p_full);
+    }
+    if (!ok) break;
+    if (!(ok = W.wait(B.o_full, of))) break;
+    of ^= 1;
+    tc_fence_after();
+    const size_t ki = static_cast<size_t>(bh) * p.T + key;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {  // 0: dV, 1: dK (times scale)
+      __nv_bfloat16* out = (part ? p.dk : p.dv) + ki * D;
+      const float f = part ? p.scale : 1.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32_wait(t_acc + part * D + 32 * c, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * f, u2f(v[2 * e + 1]) * f);
+        if (key < p.T) {
+          uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.o_empty);
+  }
+}
+
+template <int D, int KIND>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const Bars B = make_bars<D>(sbase + L::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  const int warp = threadIdx.x / 32;
+  const uint32_t tmem = bwd_setup<D>(smem, B, tmem_slot, abort_flag, warp);
+  const Waiter W{abort_flag, p.timeout_ns, &g_bwd_status};
+  if (warp == BWD_PRODUCER) {
+    if (KIND == 0)
+      bwd_producer<D, 0>(p, W, B, sbase, &tmQ, &tmDO, &tmK, &tmV);  // resident Q, dO; streamed K, V
+    else
+      bwd_producer<D, 1>(p, W, B, sbase, &tmK, &tmV, &tmQ, &tmDO);  // resident K, V; streamed Q, dO
+    __syncwarp();
+  } else if (warp == BWD_MMA) {
+    bwd_mma<D, KIND>(p, W, B, sbase, tmem);
+    __syncwarp();
+  } else {
+    if (KIND == 0)
+      bwd_dq_rows<D>(p, W, B, tmem);
+    else
+      bwd_dkdv_rows<D>(p, W, B, tmem, reinterpret_cast<float*>(smem + L::VEC_OFF));
+  }
+  bwd_teardown<D>(tmem, warp);
+}
+
+template <int D, int KIND>
+cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                       const BwdParams& p, int grid, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(fa_bwd_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdLayout<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(BWD_THREADS);
+  cfg.dynamicSmemBytes = BwdLayout<D>::SMEM;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, fa_bwd_kernel<D, KIND>, q, k, v, dout, p);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream) {
+  const size_t rows = static_cast<size_t>(p.BH) * p.T;
+  const size_t blocks = (rows + 7) / 8;
+  const int grid = static_cast<int>(blocks < static_cast<size_t>(num_sms) * 8 ? blocks : num_sms * 8);
+  if (d == 64)
+    fa_bwd_rowdot_kernel<64><<<grid, 256, 0, stream>>>(p);
+  else
+    fa_bwd_rowdot_kernel<128><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_bwd<64, 0>(q, k, v, dout, p, grid, stream) : launch_bwd<128, 0>(q, k, v, dout, p, grid, stream);
+}
+
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_bwd<64, 1>(q, k, v, dout, p, grid, stream) : launch_bwd<128, 1>(q, k, v, dout, p, grid, stream);
+}
+
+int fa_bwd_smem_bytes(int d) { return d == 64 ? BwdLayout<64>::SMEM : BwdLayout<128>::SMEM; }
+
+cudaError_t read_and_clear_bwd_status(cudaStream_t stream, unsigned int* out) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_bwd_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace fa

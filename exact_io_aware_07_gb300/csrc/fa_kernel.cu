@@ -144,46 +144,6 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
 // (b, 2G-1-b, 2G+b, ...), which pairs long causal units with short ones.
 __device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k & 1) ? (G - 1 - b) : b); }
 
-// Bounded mbarrier wait: gives up when another thread of the CTA has given up,
-// or after `limit_ns`; then it records the timeout and returns false.
-struct Waiter {
-  volatile int* abort_flag;
-  unsigned long long limit_ns;
-
-  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, true);
-  }
-  // Same, but keeps waiting after another thread gave up (used to drain work in flight).
-  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, false);
-  }
-  __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, bool honour_abort) const {
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-      if (mbar_try_wait(bar, parity)) return true;
-      if ((it & 31u) == 0) {
-        if (honour_abort && *abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
-          *abort_flag = 1;
-          atomicOr(&g_status, 1u);
-          return false;
-        }
-      }
-    }
-  }
-};
-
-// Warp-wide forms for the issuing warps: every lane waits, and the warp agrees on
-// the outcome (a lane that timed out makes the whole warp give up).
-__device__ __forceinline__ bool wait_all(const Waiter& W, uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, W.wait(bar, parity));
-}
-__device__ __forceinline__ bool drain_all(const Waiter& W, uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, W.drain(bar, parity));
-}
-
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
@@ -245,7 +205,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Waiter W{abort_flag, p.timeout_ns};
+  const Waiter W{abort_flag, p.timeout_ns, &g_status};
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer (whole warp, one lane issues)
@@ -782,7 +742,7 @@ __global__ void fa_wait_selftest_kernel(unsigned long long timeout_ns) {
     fence_mbar_init();
   }
   __syncthreads();
-  const Waiter W{&abort_flag, timeout_ns};
+  const Waiter W{&abort_flag, timeout_ns, &g_status};
   if (threadIdx.x == 0) W.wait(smem_u32(&bar), 0);
 }
 

@@ -45,4 +45,34 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 // looked up on the first call for each device, then cached.
 cudaError_t noalloc_scratch_address(int dev, void** out);
 
+// ---------------------------------------------------------------- backward pass (fa_bwd.cu)
+
+struct BwdParams {
+  const __nv_bfloat16* o;     // (B*H, T, d) forward output
+  const __nv_bfloat16* dout;  // (B*H, T, d) upstream gradient
+  const float* lse;           // (B*H, T) forward log-sum-exp (natural log)
+  float* drow;                // (B*H, T) workspace: D_t = sum_c dO_tc O_tc
+  __nv_bfloat16* dq;          // (B*H, T, d) outputs
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int BH, T, causal;
+  int nt;                     // 128-row tiles per head: ceil(T / 128)
+  int num_units;              // BH * nt
+  float scale;                // softmax scale
+  float scale_log2;           // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+// D_t = sum_c dO_tc O_tc for every row (one warp per row).
+cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream);
+// dQ: one CTA per SM, units (head, 128-row query tile), key tiles streamed.
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream);
+// dK, dV: one CTA per SM, units (head, 128-key tile), query tiles streamed.
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream);
+int fa_bwd_smem_bytes(int d);
+// Reads and clears the backward kernels' device status word (bit 0: a wait ran out).
+cudaError_t read_and_clear_bwd_status(cudaStream_t stream, unsigned int* out);
+
 }  // namespace fa

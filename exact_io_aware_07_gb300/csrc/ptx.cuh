@@ -146,6 +146,18 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "r"(taddr) : "memory");
 }
 
+// Two 32-column loads (from two column ranges of the warp's lanes) and one wait,
+// in one asm statement so that no use of the values can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32x2_wait(uint32_t taddr_a, uint32_t (&a)[32], uint32_t taddr_b,
+                                                 uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(taddr_a), "r"(taddr_b) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n\t"
@@ -315,6 +327,49 @@ __device__ __forceinline__ void tma_prefetch_l2_3d_elect(const void* tmap, int x
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];\n\t}"
       :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z) : "memory");
+}
+
+// ---------------------------------------------------------------- bounded waits
+
+// Bounded mbarrier wait: gives up when another thread of the CTA has given up,
+// or after `limit_ns`; then it records the timeout and returns false.
+struct Waiter {
+  volatile int* abort_flag;
+  unsigned long long limit_ns;
+  unsigned int* status;  // device status word: bit 0 is set when a wait runs out
+
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, true);
+  }
+  // Same, but keeps waiting after another thread gave up (used to drain work in flight).
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, false);
+  }
+  __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, bool honour_abort) const {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((it & 31u) == 0) {
+        if (honour_abort && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+          *abort_flag = 1;
+          atomicOr(status, 1u);
+          return false;
+        }
+      }
+    }
+  }
+};
+
+// Warp-wide forms for the issuing warps: every lane waits, and the warp agrees on
+// the outcome (a lane that timed out makes the whole warp give up).
+__device__ __forceinline__ bool wait_all(const Waiter& W, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, W.wait(bar, parity));
+}
+__device__ __forceinline__ bool drain_all(const Waiter& W, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, W.drain(bar, parity));
 }
 
 }  // namespace fa

@@ -27,7 +27,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 20  # value pairs generated per numpy pass (bounds temporary memory)
 
-TENSOR_IDS = {"q": 1, "k": 2, "v": 3}
+TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "do": 4}
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -180,6 +180,11 @@ def make_grouped_qkv(B: int, H: int, Hkv: int, T: int, d: int, seed: int = 0,
     k = normal_bf16_bits(seed, TENSOR_IDS["k"], B * Hkv * T * d, sigma_qk).reshape(B, Hkv, T, d)
     v = normal_bf16_bits(seed, TENSOR_IDS["v"], B * Hkv * T * d, sigma_v).reshape(B, Hkv, T, d)
     return GroupedQKV(B, H, Hkv, T, d, q, k, v)
+
+
+def make_grad_out(B: int, H: int, T: int, d: int, seed: int = 0, sigma: float = 1.0) -> np.ndarray:
+    """The upstream gradient dO ~ N(0, sigma^2), bf16 bits (B, H, T, d), for the backward pass."""
+    return normal_bf16_bits(seed, TENSOR_IDS["do"], B * H * T * d, sigma).reshape(B, H, T, d)
 
 
 # The attention workloads: shapes, masks and value distributions.

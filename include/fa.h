@@ -59,7 +59,7 @@ typedef enum {
   FA_ERR_BAD_POINTER = 10,          /* a pointer is not device memory, or its allocation is too small */
   FA_ERR_ALIAS = 11,                /* O or LSE overlaps an input or each other */
   FA_ERR_CUDA = 12,                 /* a CUDA runtime or driver query failed */
-  FA_ERR_WORKSPACE = 13             /* the split-KV workspace is missing or too small */
+  FA_ERR_WORKSPACE = 13             /* a workspace is missing or smaller than its *_workspace_bytes() */
 } fa_status;
 
 /* Largest number of key splits fa_fwd_splitkv accepts. */
@@ -121,6 +121,37 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int H, int T, int d, int causal, float scale, int num_splits,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Backward pass: the gradients of sum(dO * O) with respect to Q, K and V
+ * ("FlashAttention and Fused Kernels: Attention Without the n x n Matrix",
+ * section "Training: recompute instead of store": only O and the per-row
+ * log-sum-exp are kept from the forward pass; S and P are recomputed tile by
+ * tile).  With P = exp(scale Q K^T - LSE) (masked when causal) and
+ * D_t = sum_c dO_tc O_tc:
+ *   dV = P^T dO,   dS = P * (dO V^T - D),   dQ = scale dS K,   dK = scale dS^T Q.
+ *   q, k, v, o, dout : (B, H, T, d) bf16, contiguous, d fastest; o and lse are
+ *                      what fa_fwd returned for q, k, v, causal and scale.
+ *   lse              : (B, H, T) fp32, natural log.
+ *   dq, dk, dv       : (B, H, T, d) bf16 outputs, overwritten.
+ *   workspace        : device memory of at least fa_bwd_workspace_bytes(B, H, T)
+ *                      bytes, 16-byte aligned (it receives D; nothing in it needs
+ *                      to be set beforehand).
+ * Three kernels run in order on `stream`: D, then dQ (one unit per 128-row query
+ * tile), then dK and dV (one unit per 128-key tile); no output is accumulated
+ * across units, so the result does not depend on scheduling.
+ * Errors: as fa_fwd for the shared arguments; FA_ERR_NULL_PTR / FA_ERR_MISALIGNED
+ * / FA_ERR_BAD_POINTER for dout, dq, dk, dv; FA_ERR_WORKSPACE for a NULL or too
+ * small workspace; FA_ERR_ALIAS when an output or the workspace overlaps an input
+ * or another output.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv,
+                 int B, int H, int T, int d, int causal, float scale,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace fa_bwd needs: B * H * T * 4 bytes rounded up to 256; 0 for sizes out of range. */
+size_t fa_bwd_workspace_bytes(int B, int H, int T);
 
 /* Size of the fixed device scratch fa_fwd_splitkv_noalloc uses (32 MiB). */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

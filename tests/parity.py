@@ -91,3 +91,22 @@ def sampled_rows(T: int, seed: int, first: int = 256, last: int = 256, random: i
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+def bwd_bounds(q, k, v, do, o_fwd, causal: bool, scale: float):
+    """Exact gradients of one head and the per-element bounds the backward kernels must meet.
+
+    q, k, v, do: (T, d) float64 values of the bf16 inputs; o_fwd: the forward output the
+    kernels were given (bf16 values).  Returns ((dq, dk, dv), (bq, bk, bv)); see
+    tests/test_gpu_bwd.py for where each term comes from.
+    """
+    import oracle.backward as BW
+
+    dq, dk, dv, P, dS = BW.attention_bwd_parts(q, k, v, do, causal, scale)
+    o_err = 2 * (2.0 ** -8 * np.abs(P) @ np.abs(v) + 2.0 ** -9 * np.abs(o_fwd))
+    pe = P * (np.abs(do) * o_err).sum(axis=1)[:, None]
+    r = 4 * 2.0 ** -9
+    bv = r * (np.abs(P).T @ np.abs(do)) + 2 * 2.0 ** -9 * np.abs(dv) + 1e-6
+    bk = r * scale * (np.abs(dS).T @ np.abs(q)) + scale * (pe.T @ np.abs(q)) + 2 * 2.0 ** -9 * np.abs(dk) + 1e-6
+    bq = r * scale * (np.abs(dS) @ np.abs(k)) + scale * (pe @ np.abs(k)) + 2 * 2.0 ** -9 * np.abs(dq) + 1e-6
+    return (dq, dk, dv), (bq, bk, bv)
