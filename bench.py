@@ -368,9 +368,100 @@ def time_gqa(fa, torch, dev, g, steps):
     return sum(ms) / len(ms) / 1e3
 
 
-def run_sweep(fa, torch, dev, names, peaks, splitkv=SPLITKV_SWEEP, gqa=GQA_SWEEP):
+# backward pass: FLOPs counted as 2.5x the forward's (dV, dP, dQ, dK and the recomputed S; the
+# kernels also recompute dP and S once more, which is not counted)
+BWD_SWEEP = ["gpt2s_causal_b8h12t1024d64", "llama8b_causal_b1h32t4096d128", "llama8b_b1h32t4096d128"]
+
+
+def time_bwd(fa, torch, dev, w, steps):
+    """Device time of fa_bwd (three kernels) per step, inputs rotating past L2."""
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    qkv = fi.make_qkv(B, H, T, d, seed=0, sigma_qk=w["sigma_qk"])
+    q0, k0, v0 = device_inputs(qkv, torch, dev)
+    do0 = torch.from_numpy(fi.make_grad_out(B, H, T, d, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+    scale = 1.0 / math.sqrt(d)
+    set_bytes = 9 * q0.numel() * 2
+    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
+    sets = []
+    for s in range(nsets):
+        q, k, v, do = (x if s == 0 else x.clone() for x in (q0, k0, v0, do0))
+        o, lse = fa.attention(q, k, v, causal=causal, scale=scale)
+        sets.append((q, k, v, o, lse, do, torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, T), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(5):
+        fa.fa_bwd(*sets[i % nsets], causal, scale, ws, stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fa.fa_bwd(*sets[i % nsets], causal, scale, ws, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if fa.fa_device_status(stream) != 0:
+        raise RuntimeError("a bounded in-kernel wait ran out in the backward pass")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return sum(ms) / len(ms) / 1e3
+
+
+# e4m3 forward (d = 128): the contraction runs at the fp8 rate, so its roofline peak is the measured
+# bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+FP8_SWEEP = ["llama8b_causal_b1h32t4096d128", "llama8b_b1h32t4096d128"]
+FP8_OVER_BF16 = 2.0
+
+
+def time_fp8(fa, torch, dev, w, steps):
+    """Device time of fa_fwd_fp8 (V transpose + attention) per step, inputs rotating past L2."""
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    x = fi.make_qkv_e4m3(B, H, T, d, seed=0)
+    q0, k0, v0 = (torch.from_numpy(np.ascontiguousarray(getattr(x, n + "8"))).to(dev) for n in "qkv")
+    set_bytes = 3 * q0.numel() + 2 * q0.numel() * 2
+    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
+    sets = []
+    for s in range(nsets):
+        q, k, v = (t if s == 0 else t.clone() for t in (q0, k0, v0))
+        sets.append((q, k, v, torch.empty(B, H, T, d, dtype=torch.bfloat16, device=dev),
+                     torch.empty(B, H, T, dtype=torch.float32, device=dev)))
+    ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, T, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = 1.0 / math.sqrt(d)
+    for i in range(5):
+        fa.fa_fwd_fp8(*sets[i % nsets], causal, scale, x.descale, ws, stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fa.fa_fwd_fp8(*sets[i % nsets], causal, scale, x.descale, ws, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return sum(ms) / len(ms) / 1e3
+
+
+def run_sweep(fa, torch, dev, names, peaks, splitkv=SPLITKV_SWEEP, gqa=GQA_SWEEP, bwd=BWD_SWEEP, fp8=FP8_SWEEP):
     """Every other workload, measured the same way with fewer steps (informational)."""
     out = {}
+    for name in fp8:
+        w = fi.WORKLOADS[name]
+        f = metric_flops(w["B"], w["H"], w["T"], w["d"], w["causal"])
+        steps = int(min(2000, max(20, 0.5 / max(f / 2.0e15, 1e-6))))
+        sec = time_fp8(fa, torch, dev, w, steps)
+        peak8 = FP8_OVER_BF16 * peaks["bf16_tflops"]
+        out[f"fp8_{name}"] = {"ms_mean": round(sec * 1e3, 4), "tflops": round(f / sec / 1e12, 1),
+                              "pct_of_fp8_peak": round(100 * f / sec / 1e12 / peak8, 1),
+                              "fp8_peak_tflops": round(peak8, 1), "steps": steps,
+                              "kernels": "fa_transpose_e4m3_kernel + fa_fwd_kernel (e4m3)"}
+        torch.cuda.empty_cache()
+    for name in bwd:
+        w = fi.WORKLOADS[name]
+        f = 2.5 * metric_flops(w["B"], w["H"], w["T"], w["d"], w["causal"])
+        steps = int(min(1000, max(20, 0.5 / max(f / 0.6e15, 1e-6))))
+        sec = time_bwd(fa, torch, dev, w, steps)
+        out[f"backward_{name}"] = {"ms_mean": round(sec * 1e3, 4), "tflops": round(f / sec / 1e12, 1),
+                                   "pct_of_bf16_peak": round(100 * f / sec / 1e12 / peaks["bf16_tflops"], 1),
+                                   "steps": steps, "flops": "2.5 x forward",
+                                   "kernels": "fa_bwd_rowdot_kernel + fa_bwd_kernel (dQ) + fa_bwd_kernel (dK, dV)"}
+        torch.cuda.empty_cache()
     for name, g in gqa.items():
         f = metric_flops(g["B"], g["H"], g["T"], g["d"], g["causal"])
         steps = int(min(2000, max(20, 0.5 / max(f / 1.0e15, 1e-6))))

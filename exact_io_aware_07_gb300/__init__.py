@@ -39,7 +39,7 @@ STATUS = {
     11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA", 13: "FA_ERR_WORKSPACE",
 }
 FA_MAX_SPLITS = 256
-EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
+EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
             "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version"]
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -70,6 +70,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd.restype = i
     lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa_fwd_gqa.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa_bwd.restype = i
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i]
@@ -194,6 +198,36 @@ def attention_gqa(q, k, v, causal: bool = False, scale: float | None = None, str
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     fa_fwd_gqa(q, k, v, o, lse, causal, scale, stream)
     return o, lse
+
+
+def fa_fwd_fp8_workspace_bytes(B: int, H: int, T: int, d: int) -> int:
+    return int(load_library().fa_fwd_fp8_workspace_bytes(B, H, T, d))
+
+
+def fa_fwd_fp8(q, k, v, o, lse, causal: bool, scale: float, descales=(1.0, 1.0, 1.0), workspace=None,
+               stream=None) -> None:
+    """e4m3 Q, K, V (uint8 CUDA tensors (B, H, T, 128) holding the bytes) with per-tensor scales
+    ``descales`` = (q, k, v); O bf16 (B, H, T, 128), LSE fp32 (B, H, T).  ``workspace``: a CUDA tensor
+    of at least ``fa_fwd_fp8_workspace_bytes`` bytes (allocated here when None)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.uint8 or t.dim() != 4 or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError(f"{name} must be a contiguous uint8 (B, H, T, d) tensor of e4m3 bytes")
+    B, H, T, d = q.shape
+    if o.dtype != torch.bfloat16 or tuple(o.shape) != (B, H, T, d) or not o.is_contiguous():
+        raise ValueError("o must be a contiguous bf16 (B, H, T, d) tensor")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 (B, H, T) tensor")
+    if workspace is None:
+        workspace = torch.empty(max(1, fa_fwd_fp8_workspace_bytes(B, H, T, d)), dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    qs, ks, vs = (float(x) for x in descales)
+    code = load_library().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                     B, H, T, d, int(bool(causal)), float(scale), qs, ks, vs,
+                                     workspace.data_ptr(), nbytes, ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_fwd_fp8")
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, T: int) -> int:

@@ -130,18 +130,22 @@ fa_status validate_host(const void* q, const void* k, const void* v, const void*
   return FA_OK;
 }
 
-bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
+// 3-D view (inner, rows, B*H) of a contiguous tensor: a box (128 bytes of the inner
+// dimension x 128 rows x 1) never crosses from one head into the next, and rows past
+// `rows` read as zeros.  bf16 (d, T, B*H) views, or byte views for e4m3 tensors.
+bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int rows, int inner, bool bytes) {
   const DriverFns& fns = driver_fns();
   if (!fns.encode_tiled) return false;
-  // 3-D view (d, T, B*H): a box never crosses from one head into the next, and
-  // rows past T read as zeros.
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(T) * d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint64_t es = bytes ? 1 : 2;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * es, static_cast<cuuint64_t>(rows) * inner * es};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 128, 1};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
-  return fns.encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fns.encode_tiled(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Encoded descriptors, reused when the same tensor comes back (encoding reads no
@@ -149,25 +153,27 @@ bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d)
 struct MapCacheEntry {
   const void* base = nullptr;
   int BH = 0, T = 0, d = 0;
+  bool bytes = false;
   CUtensorMap map;
 };
 constexpr int kMapCache = 16;
 MapCacheEntry g_map_cache[kMapCache];
 std::mutex g_map_mu;
 
-bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d) {
+bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d, bool bytes = false) {
   const size_t slot = (reinterpret_cast<uintptr_t>(base) >> 8) % kMapCache;
   std::lock_guard<std::mutex> lock(g_map_mu);
   MapCacheEntry& e = g_map_cache[slot];
-  if (e.base == base && e.BH == BH && e.T == T && e.d == d) {
+  if (e.base == base && e.BH == BH && e.T == T && e.d == d && e.bytes == bytes) {
     *map = e.map;
     return true;
   }
-  if (!encode_tensor_map(map, base, BH, T, d)) return false;
+  if (!encode_tensor_map(map, base, BH, T, d, bytes)) return false;
   e.base = base;
   e.BH = BH;
   e.T = T;
   e.d = d;
+  e.bytes = bytes;
   e.map = *map;
   return true;
 }
@@ -219,6 +225,7 @@ fa_status prepare(const void* q, const void* k, const void* v, void* o, float* l
   p.nk = (T + 127) / 128;
   p.num_units = BH * p.nqb;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.v_descale = 1.f;
   p.timeout_ns = kWaitLimitNs;
   p.num_splits = 1;
   p.split_tiles = p.nk;
@@ -307,6 +314,75 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
     if (overlaps(workspace, need, x, qkv_bytes)) return FA_ERR_ALIAS;
   if (overlaps(workspace, need, lse, lse_bytes)) return FA_ERR_ALIAS;
   return launch_splitkv(pr, d, num_splits, static_cast<float*>(workspace), stream);
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int T, int d) {
+  if (B < 1 || H < 1 || T < 1 || d != 128) return 0;
+  const size_t Tp = (static_cast<size_t>(T) + 15) / 16 * 16;
+  const size_t bytes = static_cast<size_t>(B) * H * 128 * Tp;
+  return (bytes + 255) / 256 * 256;
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T, int d,
+                     int causal, float scale, float q_descale, float k_descale, float v_descale, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+  fa_status st = validate_host(q, k, v, o, lse, B, H, T, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
+  for (float x : {q_descale, k_descale, v_descale})
+    if (!std::isfinite(x) || !(x > 0.f)) return FA_ERR_BAD_SCALE;
+  const size_t need = fa_fwd_fp8_workspace_bytes(B, H, T, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return FA_ERR_MISALIGNED;
+  const int BH = B * H;
+  if (BH > 65535) return FA_ERR_BAD_SHAPE;  // one grid row of the V transpose per head
+  int dev = 0, num_sms = 0;
+  if ((st = current_device(&dev, &num_sms)) != FA_OK) return st;
+  const int Tp = (T + 15) / 16 * 16;
+  const size_t in_bytes = static_cast<size_t>(BH) * T * 128, o_bytes = static_cast<size_t>(BH) * T * 128 * 2,
+               lse_bytes = static_cast<size_t>(BH) * T * 4;
+  const struct {
+    const void* p;
+    size_t n;
+  } ins[3] = {{q, in_bytes}, {k, in_bytes}, {v, in_bytes}},
+    outs[3] = {{o, o_bytes}, {lse, lse_bytes}, {workspace, need}};
+  for (const auto& x : ins)
+    if ((st = check_device_range(x.p, x.n, dev)) != FA_OK) return st;
+  for (const auto& x : outs)
+    if ((st = check_device_range(x.p, x.n, dev)) != FA_OK) return st;
+  for (int a = 0; a < 3; ++a) {
+    for (const auto& x : ins)
+      if (overlaps(outs[a].p, outs[a].n, x.p, x.n)) return FA_ERR_ALIAS;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlaps(outs[a].p, outs[a].n, outs[b].p, outs[b].n)) return FA_ERR_ALIAS;
+  }
+  CUtensorMap tq, tk, tvt;
+  if (!make_tensor_map(&tq, q, BH, T, 128, true) || !make_tensor_map(&tk, k, BH, T, 128, true) ||
+      !make_tensor_map(&tvt, workspace, BH, 128, Tp, true))
+    return FA_ERR_CUDA;
+  fa::Params p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = BH;
+  p.H = H;
+  p.group = 1;
+  p.T = T;
+  p.causal = causal;
+  p.nqb = (T + 255) / 256;
+  p.nk = (T + 127) / 128;
+  p.num_units = BH * p.nqb;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * q_descale * k_descale * 1.4426950408889634074);
+  p.v_descale = v_descale;
+  p.timeout_ns = kWaitLimitNs;
+  p.num_splits = 1;
+  p.split_tiles = p.nk;
+  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
+  if (fa::launch_transpose_e4m3(v, workspace, BH, T, Tp, stream) != cudaSuccess ||
+      fa::launch_fa_fwd_e4m3(tq, tk, tvt, p, grid, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int T) {

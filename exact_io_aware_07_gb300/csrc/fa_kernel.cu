@@ -63,19 +63,21 @@ constexpr float LN2 = 0.693147180559945309f;
 
 __device__ unsigned int g_status;  // bit 0: a bounded wait ran out
 
-template <int D>
+// F8: Q, K and V are e4m3 bytes (d = 128 only), V read from a transposed copy (d rows of
+// keys), P packed to e4m3 for the P V product.
+template <int D, bool F8 = false>
 struct Layout {
-  static constexpr int TILE_BYTES = BM * D * 2;
-  static constexpr int BOXES = D / 64;
-  // d = 64: two units' Q tiles resident (the next unit's load overlaps the current
-  // unit); d = 128: one unit's Q tiles, the next unit's prefetched into L2.
-  static constexpr int QBUF = (D == 128) ? 1 : 2;
-  static constexpr int STAGES = (D == 128) ? 4 : 6;   // K/V ring depth (tiles)
+  static constexpr int TILE_BYTES = BM * D * (F8 ? 1 : 2);
+  static constexpr int BOXES = F8 ? 1 : D / 64;        // TMA boxes of 128-byte rows per tile
+  // d = 64 and e4m3: two units' Q tiles resident (the next unit's load overlaps the
+  // current unit); bf16 d = 128: one unit's Q tiles, the next unit's prefetched into L2.
+  static constexpr int QBUF = (D == 128 && !F8) ? 1 : 2;
+  static constexpr int STAGES = F8 ? 8 : (D == 128) ? 4 : 6;   // K/V ring depth (tiles)
   static constexpr int Q_OFF = 0;                      // [QBUF units][2 query tiles]
   static constexpr int KV_OFF = QBUF * 2 * TILE_BYTES;
   // d = 64: P_i has Tensor Memory columns of its own, so S_i(j+1) may be computed
   // while the softmax of S_i(j) runs (see the MMA issuer); d = 128: P_i overwrites S_i.
-  static constexpr bool SEP_P = (D == 64);
+  static constexpr bool SEP_P = (D == 64) && !F8;
   static constexpr int ON = D;                          // O columns per query tile in TMEM
   // d = 64: one MMA-issuing warp per query tile (warps 9, 10; warp 11 idle); d = 128: warp 9 alone
   static constexpr int THREADS = SEP_P ? 384 : 320;
@@ -147,11 +149,12 @@ __device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-template <int D, bool PARTIAL>
-__global__ void __launch_bounds__(Layout<D>::THREADS, 1)
+template <int D, bool PARTIAL, bool F8 = false>
+__global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using L = Layout<D>;
+  using L = Layout<D, F8>;
+  static_assert(!F8 || (D == 128 && !PARTIAL), "the e4m3 path is d = 128, unsplit");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -261,8 +264,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (!(ok = wait_all(W, bar_kv_empty + 8 * stage, phase ^ 1))) break;                                  \
     mbar_arrive_expect_tx_elect(bar_kv_full + 8 * stage, L::TILE_BYTES);                                  \
     _Pragma("unroll") for (int b = 0; b < L::BOXES; ++b)                                                  \
-      tma_load_3d_elect(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, (kv) == 0 ? &tmK : &tmV, b * 64, \
-                        (u.jb + (j)) * BN, kvh, bar_kv_full + 8 * stage);                                 \
+      tma_load_3d_elect(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, (kv) == 0 ? &tmK : &tmV,            \
+                        (F8 && (kv) == 1) ? (u.jb + (j)) * BN : b * 64,                                   \
+                        (F8 && (kv) == 1) ? 0 : (u.jb + (j)) * BN, kvh, bar_kv_full + 8 * stage);       \
     issued |= 1u << stage;                                                                                \
     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);                                  \
     if (++stage == L::STAGES) {                                                                           \
@@ -438,6 +442,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     {
       constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);   // S = Q K^T: both K-major
       constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, L::ON, 1);  // O += P V: V is MN-major
+      constexpr uint32_t IDESC_S8 = make_idesc_e4m3(BM, BN);     // e4m3: S = Q K^T
+      constexpr uint32_t IDESC_PV8 = make_idesc_e4m3(BM, L::ON);  // e4m3: O += P (V^T)^T, both K-major
+      constexpr int KSTEP = F8 ? 32 : 16;                        // reduction depth of one MMA
       // Descriptor halves: the address field (low 14 bits, in 16-byte units) is the
       // only part that changes, and every offset added below stays inside it.
       const uint64_t dqk = make_sdesc_sw128(sbase, 16, 1024);        // K-major tiles (Q, K)
@@ -466,19 +473,28 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   {                                                                                                       \
     const uint32_t a0 = q_lo0 + (((i) * L::TILE_BYTES) >> 4);                                             \
     const uint32_t b0 = dqk_lo + ((L::KV_OFF + (ks) * L::TILE_BYTES) >> 4);                               \
-    _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                               \
+    _Pragma("unroll") for (int kk = 0; kk < D / KSTEP; ++kk) {                                            \
       const uint32_t off = (((kk / 4) * BOX_BYTES + (kk % 4) * 32) >> 4);                                 \
-      mma_ss_elect(tmem + L::s_col(i), a0 + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);     \
+      if (F8)                                                                                             \
+        mma_f8_ss_elect(tmem + L::s_col(i), a0 + off, dqk_hi, b0 + off, dqk_hi, IDESC_S8, kk > 0 ? 1u : 0u); \
+      else                                                                                                \
+        mma_ss_elect(tmem + L::s_col(i), a0 + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);   \
     }                                                                                                     \
   }
-        // O_i (+)= P_i V over keys in steps of 16 (stage vs of the ring)
+        // O_i (+)= P_i V over keys in steps of 16 (bf16; V MN-major) or 32 (e4m3; V^T K-major),
+        // stage vs of the ring
 #define FA_ISSUE_PV(i, vs, acc)                                                                           \
   {                                                                                                       \
     const uint32_t s16 = ((vs) * L::TILE_BYTES) >> 4;                                                     \
-    const uint32_t b0 = dv_lo + (L::KV_OFF >> 4) + s16;                                                   \
-    _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                                \
-      mma_ts_elect(tmem + L::o_col(i), tmem + L::p_col(i) + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi,        \
-                  IDESC_PV, ((acc) || kk > 0) ? 1u : 0u);                                                 \
+    const uint32_t b0 = (F8 ? dqk_lo : dv_lo) + (L::KV_OFF >> 4) + s16;                                   \
+    _Pragma("unroll") for (int kk = 0; kk < BN / KSTEP; ++kk) {                                           \
+      if (F8)                                                                                             \
+        mma_f8_ts_elect(tmem + L::o_col(i), tmem + L::p_col(i) + kk * 8, b0 + ((kk * 32) >> 4), dqk_hi,    \
+                        IDESC_PV8, ((acc) || kk > 0) ? 1u : 0u);                                           \
+      else                                                                                                \
+        mma_ts_elect(tmem + L::o_col(i), tmem + L::p_col(i) + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi,      \
+                     IDESC_PV, ((acc) || kk > 0) ? 1u : 0u);                                               \
+    }                                                                                                     \
   }
 #define FA_TAKE(slot)                                                  \
   {                                                                    \
@@ -631,6 +647,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          uint32_t h8 = 0;  // e4m3: this chunk's weights summed as f16 pairs (exact inputs, 16 terms)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float x0, x1;
@@ -641,6 +658,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               fadd2(lb0, lb1, p0, p1);
             else
               fadd2(la0, la1, p0, p1);
+            if (F8) {  // four e4m3 weights per Tensor Memory column
+              const uint32_t b2 = pack_e4m3x2(p0, p1);
+              if (e & 1)
+                pk[8 * c + e / 2] |= b2 << 16;
+              else
+                pk[8 * c + e / 2] = b2;
+              h8 = add_f16x2(h8, e4m3x2_to_f16x2(b2));
+              continue;
+            }
             pk[16 * c + e] = pack_bf16x2(p0, p1);
             // sum of the bf16 weights (the two forms measure fastest at d = 64 and d = 128)
             if (L::SEP_P)  // bf16 -> fp32 is a shift / mask of the packed word, then one packed add
@@ -648,7 +674,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             else
               add_bf16x2_f32(pk[16 * c + e], lr0, lr1);
           }
-          if (!L::SEP_P) tmem_st16(t_p + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
+          if (F8) {
+            float h0, h1;
+            f16x2_to_f32(h8, h0, h1);
+            lr0 += h0;
+            lr1 += h1;
+            if (c & 1) tmem_st16(t_p + (c / 2) * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * (c / 2)));
+          } else if (!L::SEP_P) {
+            tmem_st16(t_p + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
+          }
         }
         if (L::SEP_P) {  // P_i(j-1) V_(j-1) must be done before P_i is overwritten and before O_i is rescaled
           if (j > 0) {
@@ -681,7 +715,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (!(ok = W.wait(my_o_full, of_phase))) break;
       of_phase ^= 1;
       tc_fence_after();
-      const float inv_l = 1.f / lr;
+      const float inv_l = p.v_descale / lr;  // v_descale: 1, or the e4m3 V's scale
       if (PARTIAL) {  // this split's normalised output (fp32) and its LSE
         const int s = u.jb / p.split_tiles;
         const size_t prow = static_cast<size_t>(s) * p.BH * p.T + static_cast<size_t>(u.bh) * p.T + row;
@@ -748,25 +782,74 @@ __global__ void fa_wait_selftest_kernel(unsigned long long timeout_ns) {
 
 // ---------------------------------------------------------------- host side
 
-template <int D, bool PARTIAL>
+template <int D, bool PARTIAL, bool F8 = false>
 static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                           int grid, cudaStream_t stream) {
+  using L = Layout<D, F8>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_fwd_kernel<D, PARTIAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<D>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(fa_fwd_kernel<D, PARTIAL, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(Layout<D>::THREADS);
-  cfg.dynamicSmemBytes = Layout<D>::SMEM_BYTES;
+  cfg.blockDim = dim3(L::THREADS);
+  cfg.dynamicSmemBytes = L::SMEM_BYTES;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL>, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL, F8>, q, k, v, p);
+}
+
+static_assert(Layout<128, true>::SMEM_BYTES <= MAX_SMEM_PER_CTA, "e4m3 layout exceeds the per-CTA limit");
+
+cudaError_t launch_fa_fwd_e4m3(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt, const Params& p,
+                               int grid, cudaStream_t stream) {
+  return launch<128, false, true>(q, k, vt, p, grid, stream);
+}
+
+int fa_fwd_e4m3_smem_bytes() { return Layout<128, true>::SMEM_BYTES; }
+
+// V (rows of 128 e4m3 bytes per key) -> V^T (rows of Tp bytes per channel), keys past T
+// zero: a 64 x 64 byte tile per block through shared memory, 16-byte loads and stores.
+__global__ void __launch_bounds__(256) fa_transpose_e4m3_kernel(const uint8_t* __restrict__ v,
+                                                                uint8_t* __restrict__ vt, int T, int Tp) {
+  __shared__ uint8_t tile[64][64 + 16];
+  const int bh = blockIdx.z, c0 = blockIdx.y * 64, t0 = blockIdx.x * 64;
+  const uint8_t* src = v + static_cast<size_t>(bh) * T * 128;
+  uint8_t* dst = vt + static_cast<size_t>(bh) * 128 * Tp;
+  // 64 keys x 64 channels: each thread loads 16 bytes (one key, 16 channels)
+  {
+    const int r = threadIdx.x / 4, cc = (threadIdx.x % 4) * 16;
+    const int t = t0 + r;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (t < T) x = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(t) * 128 + c0 + cc);
+    const uint8_t* b = reinterpret_cast<const uint8_t*>(&x);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) tile[cc + i][r] = b[i];
+  }
+  __syncthreads();
+  // 64 channels x 64 keys: each thread stores 16 bytes (one channel, 16 keys)
+  {
+    const int c = threadIdx.x / 4, tt = (threadIdx.x % 4) * 16;
+    if (t0 + tt < Tp) {  // Tp is a multiple of 16, so the whole 16-byte group is inside
+      uint4 x;
+      uint8_t* b = reinterpret_cast<uint8_t*>(&x);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) b[i] = tile[c][tt + i];
+      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c0 + c) * Tp + t0 + tt) = x;
+    }
+  }
+}
+
+cudaError_t launch_transpose_e4m3(const void* v, void* vt, int BH, int T, int Tp, cudaStream_t stream) {
+  const dim3 grid((Tp + 63) / 64, 2, BH);
+  fa_transpose_e4m3_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt),
+                                                      T, Tp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,

@@ -17,7 +17,8 @@ struct Params {
   int nqb;                    // 256-row query blocks per head: ceil(T / 256)
   int nk;                     // 128-key tiles per head: ceil(T / 128)
   int num_units;              // BH * nqb
-  float scale_log2;           // scale * log2(e)
+  float scale_log2;           // scale * log2(e) (e4m3: times the Q and K scales)
+  float v_descale;            // 1, or the scale of e4m3 V (the real value is the byte's value times it)
   unsigned long long timeout_ns;  // bound on every in-kernel wait
   // split-KV (partial) launches only: each row's key tiles are cut into
   // num_splits ranges of split_tiles tiles; unit w -> (band, split, bh)
@@ -29,6 +30,12 @@ struct Params {
 
 cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const Params& p, int grid, cudaStream_t stream);
+// e4m3 Q, K and a transposed e4m3 V ((B*H, d, Tp) bytes), d = 128.
+cudaError_t launch_fa_fwd_e4m3(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt, const Params& p,
+                               int grid, cudaStream_t stream);
+// V (B*H, T, 128) e4m3 -> V^T (B*H, 128, Tp) with keys Tp > T zero (Tp = T rounded up to 16).
+cudaError_t launch_transpose_e4m3(const void* v, void* vt, int BH, int T, int Tp, cudaStream_t stream);
+int fa_fwd_e4m3_smem_bytes();
 // The same kernel writing per-split partials (p.opart, p.lsepart), then the merge.
 cudaError_t launch_fa_fwd_partial(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                   const Params& p, int grid, cudaStream_t stream);
@@ -59,7 +66,8 @@ struct BwdParams {
   int nt;                     // 128-row tiles per head: ceil(T / 128)
   int num_units;              // BH * nt
   float scale;                // softmax scale
-  float scale_log2;           // scale * log2(e)
+  float scale_log2;           // scale * log2(e) (e4m3: times the Q and K scales)
+  float v_descale;            // 1, or the scale of e4m3 V (the real value is the byte's value times it)
   unsigned long long timeout_ns;
 };
 

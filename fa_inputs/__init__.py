@@ -187,6 +187,74 @@ def make_grad_out(B: int, H: int, T: int, d: int, seed: int = 0, sigma: float = 
     return normal_bf16_bits(seed, TENSOR_IDS["do"], B * H * T * d, sigma).reshape(B, H, T, d)
 
 
+# ---------------------------------------------------------------- e4m3 (OCP FP8) inputs
+
+def _e4m3_table() -> np.ndarray:
+    """Values of the 256 e4m3 codes: sign, 4 exponent bits (bias 7), 3 mantissa bits; no
+    infinities; 0x7F and 0xFF are NaN.  Subnormals (exponent 0) are m / 8 * 2^-6."""
+    vals = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        s, e, m = code >> 7, (code >> 3) & 0xF, code & 0x7
+        if e == 0xF and m == 0x7:
+            v = np.nan
+        elif e == 0:
+            v = m / 8.0 * 2.0 ** -6
+        else:
+            v = (1.0 + m / 8.0) * 2.0 ** (e - 7)
+        vals[code] = -v if s else v
+    return vals
+
+
+E4M3_VALUES = _e4m3_table()
+E4M3_MAX = 448.0
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact float64 values of e4m3 bytes."""
+    return E4M3_VALUES[np.asarray(codes, dtype=np.uint8)]
+
+
+def f64_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 code (ties to the even code), magnitudes above 448 saturated to 448."""
+    x = np.asarray(x, dtype=np.float64)
+    pos = E4M3_VALUES[:0x7F]  # 0x00 .. 0x7E: the non-negative finite values, increasing
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(pos, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - pos[lo], pos[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(x) & (code != 0), code | 0x80, code).astype(np.uint8)
+
+
+@dataclass
+class QKV8:
+    """Seeded e4m3 inputs: bytes (B, H, T, d) and one scale per tensor (real value = byte value * scale)."""
+
+    B: int
+    H: int
+    T: int
+    d: int
+    q8: np.ndarray
+    k8: np.ndarray
+    v8: np.ndarray
+    descale: tuple
+
+    def f64(self, name: str) -> np.ndarray:
+        i = "qkv".index(name)
+        return e4m3_to_f64(getattr(self, name + "8")) * self.descale[i]
+
+
+def make_qkv_e4m3(B: int, H: int, T: int, d: int, seed: int = 0, descale=(1.0, 1.0, 1.0)) -> QKV8:
+    """Q, K, V ~ N(0, 1) in real value: each tensor's N(0, 1) draw divided by its scale,
+    rounded to e4m3 (so the bytes use the format's range whatever the scale)."""
+    out = []
+    for name, sc in zip("qkv", descale):
+        z = bf16_bits_to_f64(normal_bf16_bits(seed, TENSOR_IDS[name], B * H * T * d))
+        out.append(f64_to_e4m3(z / sc).reshape(B, H, T, d))
+    return QKV8(B, H, T, d, out[0], out[1], out[2], tuple(float(x) for x in descale))
+
+
 # The attention workloads: shapes, masks and value distributions.
 WORKLOADS = {
     "tiny_causal_b1h4t256d64": dict(B=1, H=4, T=256, d=64, causal=True, sigma_qk=1.0),

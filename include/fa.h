@@ -123,6 +123,37 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Forward pass with 8-bit inputs (FlashAttention-3's FP8 mode, "FlashAttention
+ * and Fused Kernels: Attention Without the n x n Matrix", section "Four
+ * generations of FlashAttention").  Q, K and V are e4m3 bytes (OCP FP8: sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448, 0x7F / 0xFF
+ * NaN) with one scale per tensor: the real value of a byte is its e4m3 value
+ * times q_descale, k_descale or v_descale.  Both matrix products run in e4m3
+ * (tcgen05.mma kind::f8f6f4, fp32 accumulation): P is rounded to e4m3 for the
+ * P V product and O is divided by the sum of those rounded weights, so each
+ * output row is still a convex combination of value rows; LSE uses the fp32
+ * weights.  O is bf16, LSE fp32, as for fa_fwd.
+ *   q, k, v    : (B, H, T, 128) e4m3 bytes, contiguous; d must be 128.
+ *   o, lse     : as for fa_fwd.
+ *   workspace  : device memory of at least fa_fwd_fp8_workspace_bytes(B, H, T, d)
+ *                bytes, 16-byte aligned; it receives V transposed to (B, H, 128,
+ *                T rounded up to 16), keys past T zero.  Nothing in it needs to be
+ *                set beforehand.
+ * Two kernels run in order on `stream`: the transpose of V, then attention.
+ * Errors: as fa_fwd; FA_ERR_UNSUPPORTED_HEAD_DIM for d != 128, FA_ERR_BAD_SCALE
+ * for a descale that is not finite and > 0, FA_ERR_WORKSPACE, FA_ERR_ALIAS when
+ * O, LSE or the workspace overlaps an input or each other, FA_ERR_BAD_SHAPE when
+ * B * H > 65535.
+ */
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int T, int d, int causal, float scale,
+                     float q_descale, float k_descale, float v_descale,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace fa_fwd_fp8 needs: B * H * 128 * (T rounded up to 16) bytes, rounded up to 256; 0 if d != 128. */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int T, int d);
+
+/*
  * Backward pass: the gradients of sum(dO * O) with respect to Q, K and V
  * ("FlashAttention and Fused Kernels: Attention Without the n x n Matrix",
  * section "Training: recompute instead of store": only O and the per-row

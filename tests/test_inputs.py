@@ -39,3 +39,27 @@ def test_normal_moments_and_sigma():
     assert abs(y.std() - 3.0) < 0.03
     # bf16 values are exact in float64 and finite
     assert np.all(np.isfinite(x))
+
+
+def test_e4m3_codec_against_the_format():
+    """Values fixed by the OCP FP8 e4m3 definition: bias 7, 3 mantissa bits, max 448, 0x7F NaN."""
+    import math
+
+    v = fi.E4M3_VALUES
+    assert v[0x38] == 1.0 and v[0xB8] == -1.0 and v[0x00] == 0.0
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0 and math.isnan(v[0x7F]) and math.isnan(v[0xFF])
+    assert v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9 and v[0x08] == 2.0 ** -6
+    assert v[0x39] == 1.125 and v[0x40] == 2.0 and v[0x30] == 0.5
+    finite = [c for c in range(256) if not math.isnan(v[c])]
+    codes = np.array(finite, dtype=np.uint8)
+    back = fi.f64_to_e4m3(v[codes])
+    assert np.array_equal(fi.e4m3_to_f64(back), v[codes])  # every finite value round-trips (-0 -> 0 allowed)
+    # ties go to the even code, saturation at 448
+    assert fi.f64_to_e4m3(np.array([1.0625]))[0] == 0x38 and fi.f64_to_e4m3(np.array([1.1875]))[0] == 0x3A
+    assert fi.f64_to_e4m3(np.array([500.0, -1e9]))[0] == 0x7E and fi.f64_to_e4m3(np.array([-1e9]))[0] == 0xFE
+    # rounding is to the nearest value
+    x = np.random.default_rng(0).standard_normal(10000) * 30
+    q = fi.e4m3_to_f64(fi.f64_to_e4m3(x))
+    pos = np.sort(np.unique(np.abs(v[codes])))
+    nearest = pos[np.abs(np.abs(x)[:, None] - pos[None, :]).argmin(axis=1)] * np.sign(x)
+    assert np.all(np.abs(q - x) <= np.abs(nearest - x) + 1e-15)
