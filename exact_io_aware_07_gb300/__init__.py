@@ -36,10 +36,11 @@ STATUS = {
     0: "FA_OK", 1: "FA_ERR_NULL_PTR", 2: "FA_ERR_MISALIGNED", 3: "FA_ERR_BAD_SHAPE",
     4: "FA_ERR_UNSUPPORTED_HEAD_DIM", 5: "FA_ERR_BAD_SCALE", 6: "FA_ERR_NO_DEVICE_SUPPORT",
     7: "FA_ERR_LAUNCH", 8: "FA_ERR_DEVICE_TIMEOUT", 9: "FA_ERR_BAD_ARG", 10: "FA_ERR_BAD_POINTER",
-    11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA", 13: "FA_ERR_WORKSPACE",
+    11: "FA_ERR_ALIAS", 12: "FA_ERR_CUDA", 13: "FA_ERR_WORKSPACE", 14: "FA_ERR_BAD_PAGE",
 }
 FA_MAX_SPLITS = 256
-EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
+EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_fwd_paged", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_bwd",
+            "fa_bwd_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
             "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version"]
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -70,6 +71,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd.restype = i
     lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa_fwd_gqa.restype = i
+    lib.fa_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_paged.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_fp8.restype = i
     lib.fa_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
@@ -198,6 +201,32 @@ def attention_gqa(q, k, v, causal: bool = False, scale: float | None = None, str
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     fa_fwd_gqa(q, k, v, o, lse, causal, scale, stream)
     return o, lse
+
+
+def fa_fwd_paged(q, k_pages, v_pages, block_table, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """Paged K/V: k_pages, v_pages (num_pages, Hkv, 128, d) bf16; block_table (B, max_pages) int32 on the
+    device; q, o (B, H, T, d) bf16; lse (B, H, T) fp32.  Key t of batch entry b is row t % 128 of page
+    block_table[b, t // 128]."""
+    import torch
+
+    for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages), ("o", o)):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 4-D tensor")
+    B, H, T, d = q.shape
+    num_pages, Hkv, page, dk = k_pages.shape
+    if page != 128 or dk != d or v_pages.shape != k_pages.shape or tuple(o.shape) != (B, H, T, d):
+        raise ValueError("pages must be (num_pages, Hkv, 128, d), like q's d")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+            or not block_table.is_contiguous():
+        raise ValueError("block_table must be a contiguous int32 (B, max_pages) tensor")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 (B, H, T) tensor")
+    code = load_library().fa_fwd_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), block_table.data_ptr(),
+                                       o.data_ptr(), lse.data_ptr(), B, H, Hkv, T, d, int(bool(causal)),
+                                       float(scale), num_pages, block_table.shape[1],
+                                       ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_fwd_paged")
 
 
 def fa_fwd_fp8_workspace_bytes(B: int, H: int, T: int, d: int) -> int:

@@ -219,6 +219,10 @@ fa_status prepare(const void* q, const void* k, const void* v, void* o, float* l
   p.BH = BH;
   p.H = H;
   p.group = H / Hkv;
+  p.Hkv = Hkv;
+  p.block_table = nullptr;
+  p.max_pages = 0;
+  p.num_pages = 0;
   p.T = T;
   p.causal = causal;
   p.nqb = (T + 255) / 256;
@@ -270,6 +274,71 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
   if (st != FA_OK) return st;
   const int grid = pr.p.num_units < pr.num_sms ? pr.p.num_units : pr.num_sms;
   if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, pr.p, grid, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table, void* o,
+                       float* lse, int B, int H, int Hkv, int T, int d, int causal, float scale, int num_pages,
+                       int max_pages, cudaStream_t stream) {
+  fa_status st = validate_host(q, k_pages, v_pages, o, lse, B, H, T, d, causal, scale);
+  if (st != FA_OK) return st;
+  if (!block_table) return FA_ERR_NULL_PTR;
+  if (reinterpret_cast<uintptr_t>(block_table) % 4 != 0) return FA_ERR_MISALIGNED;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_BAD_SHAPE;
+  const int nk = (T + 127) / 128;
+  if (num_pages < 1 || max_pages < nk || static_cast<long long>(num_pages) * Hkv >= INT_MAX ||
+      static_cast<long long>(B) * max_pages > INT_MAX)
+    return FA_ERR_BAD_SHAPE;
+  int dev = 0, num_sms = 0;
+  if ((st = current_device(&dev, &num_sms)) != FA_OK) return st;
+  const int BH = B * H;
+  const size_t q_bytes = static_cast<size_t>(BH) * T * d * 2, lse_bytes = static_cast<size_t>(BH) * T * 4;
+  const size_t pool_bytes = static_cast<size_t>(num_pages) * Hkv * 128 * d * 2;
+  const size_t table_bytes = static_cast<size_t>(B) * max_pages * 4;
+  const struct {
+    const void* p;
+    size_t n;
+  } ins[4] = {{q, q_bytes}, {k_pages, pool_bytes}, {v_pages, pool_bytes}, {block_table, table_bytes}},
+    outs[2] = {{o, q_bytes}, {lse, lse_bytes}};
+  for (const auto& x : ins)
+    if ((st = check_device_range(x.p, x.n, dev)) != FA_OK) return st;
+  for (const auto& x : outs)
+    if ((st = check_device_range(x.p, x.n, dev)) != FA_OK) return st;
+  for (const auto& x : ins)
+    if (overlaps(o, q_bytes, x.p, x.n) || overlaps(lse, lse_bytes, x.p, x.n)) return FA_ERR_ALIAS;
+  if (overlaps(o, q_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
+  Prepared pr;
+  pr.dev = dev;
+  pr.num_sms = num_sms;
+  // page pools as (d, 128 rows, num_pages * Hkv): one TMA box is one page of one head
+  if (!make_tensor_map(&pr.tq, q, BH, T, d) || !make_tensor_map(&pr.tk, k_pages, num_pages * Hkv, 128, d) ||
+      !make_tensor_map(&pr.tv, v_pages, num_pages * Hkv, 128, d))
+    return FA_ERR_CUDA;
+  fa::Params& p = pr.p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = BH;
+  p.H = H;
+  p.group = H / Hkv;
+  p.Hkv = Hkv;
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.T = T;
+  p.causal = causal;
+  p.nqb = (T + 255) / 256;
+  p.nk = nk;
+  p.num_units = BH * p.nqb;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.v_descale = 1.f;
+  p.timeout_ns = kWaitLimitNs;
+  p.num_splits = 1;
+  p.split_tiles = p.nk;
+  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
+  if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, p, grid, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
@@ -366,6 +435,8 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
   p.BH = BH;
   p.H = H;
   p.group = 1;
+  p.Hkv = H;
+  p.block_table = nullptr;
   p.T = T;
   p.causal = causal;
   p.nqb = (T + 255) / 256;
@@ -470,6 +541,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_BAD_POINTER: return "a pointer is not device memory of the current device, or its allocation is too small";
     case FA_ERR_ALIAS: return "an output overlaps an input or the other output";
     case FA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case FA_ERR_BAD_PAGE: return "a block-table entry named a page outside the pool (its keys read as zeros)";
     case FA_ERR_WORKSPACE: return "the workspace is missing or smaller than the size its *_workspace_bytes() gives";
   }
   return "unknown status";
@@ -484,7 +556,7 @@ fa_status fa_device_status(cudaStream_t stream, int* out) {
     return FA_ERR_CUDA;
   }
   word |= bwd;
-  *out = word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+  *out = (word & 2u) ? FA_ERR_BAD_PAGE : (word & 1u) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
   return FA_OK;
 }
 

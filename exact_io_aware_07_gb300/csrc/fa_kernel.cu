@@ -231,6 +231,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (nmax == 0) continue;  // an empty key split: no role touches it
         // the K/V head this query head reads (query heads share K/V heads in groups)
         const int kvh = p.group == 1 ? u.bh : (u.bh / p.H) * (p.H / p.group) + (u.bh % p.H) / p.group;
+        // paged K/V: the batch entry's block table row (logical 128-key page -> physical page)
+        const int* pages = p.block_table ? p.block_table + static_cast<size_t>(u.bh / p.H) * p.max_pages : nullptr;
         const int qb = nu % L::QBUF;
         const uint32_t qpar = (nu / L::QBUF) & 1;
         if (!(ok = wait_all(W, bar_q_empty + 8 * qb, qpar ^ 1))) break;
@@ -262,11 +264,22 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #define FA_LOAD(kv, j)                                                                                    \
   {                                                                                                       \
     if (!(ok = wait_all(W, bar_kv_empty + 8 * stage, phase ^ 1))) break;                                  \
+    /* paged: the tile is one whole page, row 0 of (page, K/V head) in the page pool */                   \
+    int row0 = (u.jb + (j)) * BN, head = kvh;                                                             \
+    if (pages) {                                                                                          \
+      int pg = pages[u.jb + (j)];                                                                         \
+      if (pg < 0 || pg >= p.num_pages) { /* out of the pool: read zeros and report it */                  \
+        if ((threadIdx.x & 31) == 0) atomicOr(&g_status, 2u);                                             \
+        pg = p.num_pages;                                                                                 \
+      }                                                                                                   \
+      row0 = 0;                                                                                           \
+      head = pg * p.Hkv + kvh % p.Hkv;                                                                    \
+    }                                                                                                     \
     mbar_arrive_expect_tx_elect(bar_kv_full + 8 * stage, L::TILE_BYTES);                                  \
     _Pragma("unroll") for (int b = 0; b < L::BOXES; ++b)                                                  \
       tma_load_3d_elect(kv_smem + stage * L::TILE_BYTES + b * BOX_BYTES, (kv) == 0 ? &tmK : &tmV,            \
                         (F8 && (kv) == 1) ? (u.jb + (j)) * BN : b * 64,                                   \
-                        (F8 && (kv) == 1) ? 0 : (u.jb + (j)) * BN, kvh, bar_kv_full + 8 * stage);       \
+                        (F8 && (kv) == 1) ? 0 : row0, head, bar_kv_full + 8 * stage);                   \
     issued |= 1u << stage;                                                                                \
     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);                                  \
     if (++stage == L::STAGES) {                                                                           \

@@ -12,6 +12,12 @@ struct Params {
   int BH;                     // batch * query heads
   int H;                      // query heads per batch entry
   int group;                  // query heads per K/V head (1 = multi-head; H / H_kv with grouped K/V)
+  int Hkv;                    // K/V heads per batch entry (H / group)
+  // paged K/V (block_table != nullptr): K and V are pools of 128-key pages, (num_pages, Hkv, 128, d);
+  // key tile j of batch entry b is page block_table[b * max_pages + j]
+  const int* block_table;
+  int max_pages;
+  int num_pages;
   int T;                      // sequence length
   int causal;                 // 0 or 1
   int nqb;                    // 256-row query blocks per head: ceil(T / 256)

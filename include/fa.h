@@ -59,7 +59,8 @@ typedef enum {
   FA_ERR_BAD_POINTER = 10,          /* a pointer is not device memory, or its allocation is too small */
   FA_ERR_ALIAS = 11,                /* O or LSE overlaps an input or each other */
   FA_ERR_CUDA = 12,                 /* a CUDA runtime or driver query failed */
-  FA_ERR_WORKSPACE = 13             /* a workspace is missing or smaller than its *_workspace_bytes() */
+  FA_ERR_WORKSPACE = 13,            /* a workspace is missing or smaller than its *_workspace_bytes() */
+  FA_ERR_BAD_PAGE = 14              /* (device) a block-table entry was outside the page pool */
 } fa_status;
 
 /* Largest number of key splits fa_fwd_splitkv accepts. */
@@ -121,6 +122,30 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int H, int T, int d, int causal, float scale, int num_splits,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Forward pass with K and V in a pool of fixed-size pages ("FlashAttention and
+ * Fused Kernels: Attention Without the n x n Matrix", section "Paged caches":
+ * the key/value cache is kept in fixed-size blocks found through a block
+ * table).  Pages hold 128 keys.  Key t of batch entry b (and K/V head g) is row
+ * t % 128 of page block_table[b * max_pages + t / 128] of head g.  The result is
+ * exactly fa_fwd_gqa's on the K and V those pages hold.
+ *   q, o, lse   : as for fa_fwd_gqa ((B, H, T, d) bf16, (B, H, T) fp32).
+ *   k_pages,
+ *   v_pages     : (num_pages, Hkv, 128, d) bf16, contiguous, d fastest.  Rows of
+ *                 the last page past T must hold finite values (they are masked
+ *                 out, but V's rows are still multiplied by zero weights).
+ *   block_table : (B, max_pages) int32, device memory; entries 0 .. ceil(T/128)-1
+ *                 of each row are read.  An entry outside [0, num_pages) makes
+ *                 that page read as zeros and sets FA_ERR_BAD_PAGE in the device
+ *                 status word (fa_device_status).
+ *   Hkv, the rest as for fa_fwd_gqa; max_pages >= ceil(T / 128), num_pages >= 1.
+ * Errors: as fa_fwd_gqa; FA_ERR_NULL_PTR for a NULL block table,
+ * FA_ERR_BAD_SHAPE for max_pages < ceil(T / 128) or num_pages < 1.
+ */
+fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                       void* o, float* lse, int B, int H, int Hkv, int T, int d, int causal, float scale,
+                       int num_pages, int max_pages, cudaStream_t stream);
 
 /*
  * Forward pass with 8-bit inputs (FlashAttention-3's FP8 mode, "FlashAttention
@@ -225,7 +250,8 @@ const char* fa_status_string(fa_status s);
 /*
  * Reads and clears the device status word that kernels of this library set
  * when a bounded wait runs out.  Synchronises `stream` first.  *out receives
- * FA_OK or FA_ERR_DEVICE_TIMEOUT.  Returns FA_ERR_CUDA if the copy fails.
+ * FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_BAD_PAGE (fa_fwd_paged met a page
+ * outside its pool; reported first).  Returns FA_ERR_CUDA if the copy fails.
  */
 fa_status fa_device_status(cudaStream_t stream, int* out);
 
