@@ -515,6 +515,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int warp = threadIdx.x / 32;
   const uint32_t tmem = bwd_setup<D>(smem, B, tmem_slot, abort_flag, warp);
   const Waiter W{abort_flag, p.timeout_ns, &g_bwd_status};
+  // the set-up above overlaps the previous kernel's tail; memory is read only after it has finished
+  pdl_launch_dependents();
+  pdl_wait();
   if (warp == BWD_PRODUCER) {
     if (KIND == 0)
       bwd_producer<D, 0>(p, W, B, sbase, &tmQ, &tmDO, &tmK, &tmV);  // resident Q, dO; streamed K, V
@@ -551,6 +554,11 @@ cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   cfg.blockDim = dim3(BWD_THREADS);
   cfg.dynamicSmemBytes = BwdLayout<D>::SMEM;
   cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fa_bwd_kernel<D, KIND>, q, k, v, dout, p);
 }
 

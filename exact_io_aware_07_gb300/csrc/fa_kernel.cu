@@ -209,6 +209,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.timeout_ns, &g_status};
+  // the set-up above overlaps the previous kernel's tail; inputs are read only after it has finished
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer (whole warp, one lane issues)
@@ -814,6 +817,11 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
   cfg.blockDim = dim3(L::THREADS);
   cfg.dynamicSmemBytes = L::SMEM_BYTES;
   cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL, F8>, q, k, v, p);
 }
 

@@ -329,6 +329,16 @@ __device__ __forceinline__ void tma_prefetch_l2_3d_elect(const void* tmap, int x
       :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this one depends on (the previous kernel on the stream,
+// when launched with programmatic stream serialization) have completed and their
+// memory is visible; a no-op otherwise.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream start launching (it still waits in pdl_wait()
+// for this grid to complete before it touches memory).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- 8-bit (e4m3) operands
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4 with e4m3 A and B (format code 0
