@@ -19,11 +19,12 @@
 // five) so that every product takes its A operand from Tensor Memory with the
 // rows it needs on the lanes, and no partial sum crosses CTAs.
 //
-// Roles (192 threads, one CTA per SM, persistent over work units):
-//   warps 0-3  one TMEM lane (one row of the unit's 128-row tile) per thread
-//   warp 4     TMA producer: the unit's two resident tiles, then the streamed
+// Roles (320 threads, one CTA per SM, persistent over work units):
+//   warps 0-7  row warps: one TMEM lane (one row of the unit's 128-row tile) per
+//              thread, warps w and w + 4 splitting the row's 128 columns
+//   warp 8     TMA producer: the unit's two resident tiles, then the streamed
 //              tiles through a ring
-//   warp 5     Tensor Memory allocator and tcgen05.mma issuer (whole warp,
+//   warp 9     Tensor Memory allocator and tcgen05.mma issuer (whole warp,
 //              elect.sync picks the issuing lane)
 // Every mbarrier wait is bounded; on expiry the kernel records it in its
 // status word and unwinds, as the forward kernel does.
@@ -38,9 +39,10 @@ namespace fa {
 namespace {
 
 constexpr int BT = 128;  // rows per tile (queries or keys)
-constexpr int BWD_THREADS = 192;
-constexpr int BWD_PRODUCER = 4;
-constexpr int BWD_MMA = 5;
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_PRODUCER = 8;
+constexpr int BWD_MMA = 9;
+constexpr int ROW_WARPS = 8;  // two per TMEM lane quarter, each taking half of the 128 columns
 constexpr int BOX = 128 * 128;  // one TMA box: 128 rows x 64 bf16, 128-byte swizzle
 constexpr float LOG2E = 1.4426950408889634074f;
 
@@ -56,21 +58,39 @@ struct BwdLayout {
   static constexpr int VEC_OFF = RING_OFF + STAGES * TILE;  // [2 buffers][LSE*log2e, D][128] fp32
   static constexpr int BAR_OFF = VEC_OFF + 2 * 2 * BT * 4;
   // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2]
-  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2;
+  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4;  // + s_free, dp_full, dp_free, pv_done
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
 };
 static_assert(BwdLayout<128>::SMEM <= 232448 && BwdLayout<64>::SMEM <= 232448, "shared memory over the limit");
 
 // Tensor Memory columns (512 allocated):
-//   dQ kernel:    S [0,128)    dP [128,256)    dQ [256,256+d)
-//   dK/dV kernel: S^T [0,128)  dP^T [128,256)  dV [256,256+d)  dK [256+d,256+2d)
-// P / dS (bf16 pairs) are written over the first 64 columns of S / dP.
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256;
+//   dQ kernel:         S [0,128)    dP [128,256)    dQ [256,256+d)  dS [384,448)
+//   dK/dV kernel d=64: S^T [0,128)  dP^T [128,256)  dV [256,320)  dK [320,384)  P^T [384,448)  dS^T [448,512)
+//   dK/dV kernel d=128: S^T, dP^T as above, dV [256,384), dK [384,512); P^T and dS^T are
+//     written over the first 64 columns of S^T and dP^T.
+// With P / dS in columns of their own (SPLIT), the next step's S and dP are issued as soon
+// as the row warps have read this step's, so the products overlap the row-warp work.
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256, COL_BUF = 384;
+template <int D, int KIND>
+struct BwdSched {
+  static constexpr bool SPLIT = (KIND == 0) || (D == 64);
+  // Packed (bf16-pair) column of the 16-wide K step kk of P / dS, relative to COL_P / COL_DS.
+  // The row warps of column half h write pairs for columns [64h, 64h + 64): contiguous in their
+  // own buffers (SPLIT), or over the first half of the S / dP columns they read themselves.
+  static __device__ __forceinline__ constexpr uint32_t a_col(int kk) {
+    return SPLIT ? uint32_t(kk) * 8u : uint32_t(kk / 4) * 64u + uint32_t(kk % 4) * 8u;
+  }
+  static __device__ __forceinline__ constexpr uint32_t half_col(int h) { return SPLIT ? 32u * h : 64u * h; }
+  // where the row warps put P (dK/dV kernel) and dS (both kernels)
+  static constexpr uint32_t COL_P = SPLIT ? COL_BUF : COL_S;
+  static constexpr uint32_t COL_DS = SPLIT ? (KIND == 0 ? COL_BUF : COL_BUF + 64) : COL_DP;
+};
 
 struct Bars {
   uint32_t res_full, res_empty, ring_full, ring_empty, s_full, p_full, o_full, o_empty, done;
   uint32_t vec_full;  // [2]: the per-step LSE / D vectors of the dK/dV kernel are in shared memory
+  uint32_t s_free, dp_full, dp_free, pv_done;  // SPLIT schedule
 };
 
 template <int D>
@@ -88,6 +108,10 @@ __device__ __forceinline__ Bars make_bars(uint32_t base) {
   b.o_empty = x + 24;
   b.done = x + 32;
   b.vec_full = x + 40;
+  b.s_free = x + 56;
+  b.dp_full = x + 64;
+  b.dp_free = x + 72;
+  b.pv_done = x + 80;
   return b;
 }
 
@@ -134,12 +158,16 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint
       mbar_init(B.ring_empty + 8 * s, 1);
     }
     mbar_init(B.s_full, 1);
-    mbar_init(B.p_full, 4);
+    mbar_init(B.p_full, ROW_WARPS);
     mbar_init(B.o_full, 1);
-    mbar_init(B.o_empty, 4);
+    mbar_init(B.o_empty, ROW_WARPS);
     mbar_init(B.done, 1);
-    mbar_init(B.vec_full, 128);
-    mbar_init(B.vec_full + 8, 128);
+    mbar_init(B.vec_full, 32 * ROW_WARPS);
+    mbar_init(B.vec_full + 8, 32 * ROW_WARPS);
+    mbar_init(B.s_free, ROW_WARPS);
+    mbar_init(B.dp_full, 1);
+    mbar_init(B.dp_free, ROW_WARPS);
+    mbar_init(B.pv_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -241,12 +269,19 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
 }
 
 // MMA issuer (whole warp, one lane issues).
-//   KIND 0: S = Q K^T, dP = dO V^T; after the softmax warps wrote dS: dQ += dS K.
+//   KIND 0: S = Q K^T, dP = dO V^T; after the row warps wrote dS: dQ += dS K.
 //   KIND 1: S^T = K Q^T, dP^T = V dO^T; after P^T, dS^T: dV += P^T dO, dK += dS^T Q.
+// SPLIT schedule (P / dS in columns of their own): per step t the warp issues
+//   S(t+1) once the row warps have read S(t) (s_free), dP(t+1) once they have read
+//   dP(t) (dp_free), and the gradient products of step t once P / dS are written
+//   (p_full), committing pv_done, which the row warps wait on before they overwrite
+//   P / dS.  Otherwise P / dS are written over S / dP, and step t+1's products follow
+//   step t's gradient products.
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t sbase,
                                         uint32_t tmem) {
   using L = BwdLayout<D>;
+  using SC = BwdSched<D, KIND>;
   constexpr uint32_t IDESC_S = make_idesc_bf16(BT, BT, 0);  // both operands K-major (d contiguous)
   constexpr uint32_t IDESC_G = make_idesc_bf16(BT, D, 1);   // B MN-major: rows of d contiguous elements
   const uint64_t dk = make_sdesc_sw128(sbase, 16, 1024);
@@ -255,16 +290,8 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
   const uint32_t dm_lo = uint32_t(dm), dm_hi = uint32_t(dm >> 32);
   const int G = gridDim.x;
   int stage = 0, nu = 0;
-  uint32_t phase = 0, pf = 0, oe = 0;
+  uint32_t phase = 0, pf = 0, oe = 0, sfr = 0, dpf = 0;
   bool ok = true;
-  for (int k = 0; ok && k * G < p.num_units; ++k) {
-    const int w = bwd_unit_of(k, blockIdx.x, G);
-    if (w >= p.num_units) continue;
-    int bh, rt, first, n;
-    bwd_decode<KIND>(p, w, bh, rt, first, n);
-    if (!(ok = wait_all(W, B.res_full, nu & 1))) break;
-    ++nu;
-    tc_fence_after();
 #define BWD_TAKE(slot)                                                   \
   {                                                                      \
     slot = stage;                                                        \
@@ -275,197 +302,250 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
     }                                                                    \
     tc_fence_after();                                                    \
   }
+#define BWD_WAIT(bar, par)                                  \
+  {                                                         \
+    if (!(ok = wait_all(W, bar, par))) break;               \
+    par ^= 1;                                               \
+    tc_fence_after();                                       \
+  }
+// [resident tile r] x [streamed tile in stage st]^T into Tensor Memory column col
+#define BWD_SCORE(col, r, st)                                                                              \
+  {                                                                                                        \
+    _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                                \
+      const uint32_t off = ((kk / 4) * BOX + (kk % 4) * 32) >> 4;                                          \
+      mma_ss_elect(tmem + (col), dk_lo + ((L::RES_OFF + (r) * L::TILE) >> 4) + off, dk_hi,                  \
+                   dk_lo + ((L::RING_OFF + (st) * L::TILE) >> 4) + off, dk_hi, IDESC_S, kk > 0 ? 1u : 0u);   \
+    }                                                                                                      \
+  }
+// accumulator col += (bf16 pairs at column a) x [streamed tile in stage st] (MN-major)
+#define BWD_GRAD(col, a, st, acc0)                                                                         \
+  {                                                                                                        \
+    _Pragma("unroll") for (int kk = 0; kk < BT / 16; ++kk)                                                 \
+      mma_ts_elect(tmem + (col), tmem + (a) + SC::a_col(kk), dm_lo + ((L::RING_OFF + (st) * L::TILE + kk * 2048) >> 4), \
+                   dm_hi, IDESC_G, (acc0) | (kk > 0 ? 1u : 0u));                                           \
+  }
+  for (int k = 0; ok && k * G < p.num_units; ++k) {
+    const int w = bwd_unit_of(k, blockIdx.x, G);
+    if (w >= p.num_units) continue;
+    int bh, rt, first, n;
+    bwd_decode<KIND>(p, w, bh, rt, first, n);
+    if (!(ok = wait_all(W, B.res_full, nu & 1))) break;
+    ++nu;
+    tc_fence_after();
+    int s0 = 0, s1 = 0;  // ring stages of the current step's two streamed tiles
+    if (SC::SPLIT) {
+      do {  // step 0's two products
+        BWD_TAKE(s0);
+        {
+          uint32_t par = sfr ^ 1;
+          BWD_WAIT(B.s_free, par);
+          sfr ^= 1;
+        }
+        BWD_SCORE(COL_S, 0, s0);
+        mma_commit_elect(B.s_full);
+        BWD_TAKE(s1);
+        {
+          uint32_t par = dpf ^ 1;
+          BWD_WAIT(B.dp_free, par);
+          dpf ^= 1;
+        }
+        BWD_SCORE(COL_DP, 1, s1);
+        mma_commit_elect(B.dp_full);
+      } while (0);
+      if (!ok) break;
+    }
     for (int t = 0; t < n; ++t) {
-      int s0 = 0, s1 = 0;  // ring stages of this step's two streamed tiles
-      BWD_TAKE(s0);
-      BWD_TAKE(s1);
-      // the two score-like products: [resident tile 0] x [streamed tile 0]^T, [resident 1] x [streamed 1]^T
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = ((kk / 4) * BOX + (kk % 4) * 32) >> 4;
-        mma_ss_elect(tmem + COL_S, dk_lo + (L::RES_OFF >> 4) + off, dk_hi,
-                     dk_lo + ((L::RING_OFF + s0 * L::TILE) >> 4) + off, dk_hi, IDESC_S, kk > 0 ? 1u : 0u);
+      int n0 = -1, n1 = -1;
+      if (!SC::SPLIT) {
+        BWD_TAKE(s0);
+        BWD_TAKE(s1);
+        BWD_SCORE(COL_S, 0, s0);
+        BWD_SCORE(COL_DP, 1, s1);
+        mma_commit_elect(B.s_full);
+      } else if (t + 1 < n) {  // the next step's products, as soon as this step's have been read
+        BWD_TAKE(n0);
+        {
+          uint32_t par = sfr ^ 1;
+          BWD_WAIT(B.s_free, par);
+          sfr ^= 1;
+        }
+        BWD_SCORE(COL_S, 0, n0);
+        mma_commit_elect(B.s_full);
+        BWD_TAKE(n1);
+        {
+          uint32_t par = dpf ^ 1;
+          BWD_WAIT(B.dp_free, par);
+          dpf ^= 1;
+        }
+        BWD_SCORE(COL_DP, 1, n1);
+        mma_commit_elect(B.dp_full);
       }
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = ((kk / 4) * BOX + (kk % 4) * 32) >> 4;
-        mma_ss_elect(tmem + COL_DP, dk_lo + ((L::RES_OFF + L::TILE) >> 4) + off, dk_hi,
-                     dk_lo + ((L::RING_OFF + s1 * L::TILE) >> 4) + off, dk_hi, IDESC_S, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_elect(B.s_full);
       if (t == 0) {
-        if (!(ok = wait_all(W, B.o_empty, oe ^ 1))) break;
+        uint32_t par = oe ^ 1;
+        BWD_WAIT(B.o_empty, par);
         oe ^= 1;
       }
-      if (!(ok = wait_all(W, B.p_full, pf))) break;
-      pf ^= 1;
-      tc_fence_after();
+      BWD_WAIT(B.p_full, pf);
       const uint32_t acc0 = t > 0 ? 1u : 0u;
       if (KIND == 0) {
-        // dQ += dS K_j: A = dS (bf16 pairs over S), B = K_j (streamed tile 0) MN-major
-#pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)
-          mma_ts_elect(tmem + COL_ACC, tmem + COL_S + kk * 8,
-                       dm_lo + ((L::RING_OFF + s0 * L::TILE + kk * 2048) >> 4), dm_hi, IDESC_G, acc0 | (kk > 0));
+        BWD_GRAD(COL_ACC, SC::COL_DS, s0, acc0);  // dQ += dS K_j
       } else {
-        // dV += P^T dO_i (B = streamed tile 1), dK += dS^T Q_i (B = streamed tile 0)
-#pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)
-          mma_ts_elect(tmem + COL_ACC, tmem + COL_S + kk * 8,
-                       dm_lo + ((L::RING_OFF + s1 * L::TILE + kk * 2048) >> 4), dm_hi, IDESC_G, acc0 | (kk > 0));
-#pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)
-          mma_ts_elect(tmem + COL_ACC + D, tmem + COL_DP + kk * 8,
-                       dm_lo + ((L::RING_OFF + s0 * L::TILE + kk * 2048) >> 4), dm_hi, IDESC_G, acc0 | (kk > 0));
+        BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);       // dV += P^T dO_i
+        BWD_GRAD(COL_ACC + D, SC::COL_DS, s0, acc0);  // dK += dS^T Q_i
       }
+      if (SC::SPLIT) mma_commit_elect(B.pv_done);
       mma_commit_elect(B.ring_empty + 8 * s0);
       mma_commit_elect(B.ring_empty + 8 * s1);
       if (t + 1 == n) {
         mma_commit_elect(B.res_empty);
         mma_commit_elect(B.o_full);
       }
+      if (SC::SPLIT) {
+        s0 = n0;
+        s1 = n1;
+      }
     }
-#undef BWD_TAKE
   }
+#undef BWD_TAKE
+#undef BWD_WAIT
+#undef BWD_SCORE
+#undef BWD_GRAD
   // every MMA and commit arrival has landed before Tensor Memory is freed
   mma_commit_elect(B.done);
   drain_all(W, B.done, 0);
 }
 
-// Softmax-side warps of the dQ kernel: thread = query row.  For each key tile:
-// P = exp(S - LSE) (masked entries 0), dS = P (dP - D) in bf16 over S; at the end
-// of the unit dQ = scale * (sum dS K) in bf16.
-template <int D>
-__device__ __forceinline__ void bwd_dq_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem) {
+// Row warps: eight, two per TMEM lane quarter; warp w holds row 32 (w % 4) + lane of
+// the unit's 128-row tile and columns [64h, 64h + 64) with h = w / 4.  Each step:
+//   P = exp(S - LSE) with masked entries 0, packed to bf16 pairs;
+//   dS = P (dP - D), packed to bf16 pairs;
+// and the pairs go to Tensor Memory for the gradient products.  With the SPLIT
+// schedule S and dP are read whole before anything is written (s_free and dp_free
+// let the MMA warp overwrite them with the next step's), and P / dS go to their own
+// columns once the previous step's gradient products are done (pv_done).
+// KIND 0 (dQ): the row is a query; LSE and D are per row, the mask runs along keys.
+// KIND 1 (dK, dV): the row is a key; LSE and D are per column (query), read from the
+// step's vectors in shared memory (every lane reads the same word), and P^T is
+// stored as well as dS^T.
+template <int D, int KIND>
+__device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem,
+                                         float* vec) {
+  using SC = BwdSched<D, KIND>;
+  constexpr int HC = BT / 2;  // columns per half
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int r = warp * 32 + lane;
-  const uint32_t lane_off = uint32_t(warp * 32) << 16;
-  const uint32_t t_s = tmem + lane_off + COL_S, t_dp = tmem + lane_off + COL_DP, t_acc = tmem + lane_off + COL_ACC;
+  const int q4 = warp % 4, h = warp / 4;
+  const int r = q4 * 32 + lane;
+  const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+  const uint32_t t_s = tmem + lane_off + COL_S + HC * h, t_dp = tmem + lane_off + COL_DP + HC * h;
+  const uint32_t t_acc = tmem + lane_off + COL_ACC;
+  const uint32_t t_p = tmem + lane_off + SC::COL_P + SC::half_col(h);
+  const uint32_t t_ds = tmem + lane_off + SC::COL_DS + SC::half_col(h);
   const float sl2 = p.scale_log2;
   const int G = gridDim.x;
-  uint32_t sf = 0, of = 0;
+  uint32_t sf = 0, dpf = 0, pvd = 0, of = 0;
+  int it = 0;  // steps so far (vector buffer, first pv_done wait)
   bool ok = true;
   for (int k = 0; ok && k * G < p.num_units; ++k) {
     const int w = bwd_unit_of(k, blockIdx.x, G);
     if (w >= p.num_units) continue;
     int bh, rt, first, n;
-    bwd_decode<0>(p, w, bh, rt, first, n);
-    const int q0 = rt * BT, row = q0 + r;
+    bwd_decode<KIND>(p, w, bh, rt, first, n);
+    const int r0 = rt * BT, row = r0 + r;  // this thread's query (KIND 0) or key (KIND 1)
     const size_t ri = static_cast<size_t>(bh) * p.T + row;
-    const float lse2 = row < p.T ? p.lse[ri] * LOG2E : 0.f;
-    const float drow = row < p.T ? p.drow[ri] : 0.f;
-    for (int j = 0; j < n; ++j) {
-      if (!(ok = W.wait(B.s_full, sf))) break;
-      sf ^= 1;
-      tc_fence_after();
-      const int k0 = j * BT;
-      // keys this row may use in the tile: all, or up to the diagonal / the end of the sequence
-      int lim = BT;
-      if ((p.causal && k0 + BT - 1 > q0) || k0 + BT > p.T) {
-        lim = p.T - k0;
-        if (p.causal) lim = min(lim, row - k0 + 1);
-      }
-#pragma unroll
-      for (int c = 0; c < BT / 32; ++c) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32x2_wait(t_s + 32 * c, sv, t_dp + 32 * c, dv);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = 32 * c + 2 * e;
-          float p0 = ex2_approx(fmaf(u2f(sv[2 * e]), sl2, -lse2));
-          float p1 = ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, -lse2));
-          if (c0 >= lim) p0 = 0.f;
-          if (c0 + 1 >= lim) p1 = 0.f;
-          pk[e] = pack_bf16x2(p0 * (u2f(dv[2 * e]) - drow), p1 * (u2f(dv[2 * e + 1]) - drow));
-        }
-        tmem_st16(t_s + 16 * c, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B.p_full);
-    }
-    if (!ok) break;
-    if (!(ok = W.wait(B.o_full, of))) break;
-    of ^= 1;
-    tc_fence_after();
-    __nv_bfloat16* out = p.dq + ri * D;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32_wait(t_acc + 32 * c, v);
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * p.scale, u2f(v[2 * e + 1]) * p.scale);
-      if (row < p.T) {
-        uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-      }
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(B.o_empty);
-  }
-}
-
-// Softmax-side warps of the dK/dV kernel: thread = key row.  For each query tile:
-// P^T = exp(S^T - LSE) and dS^T = P^T (dP^T - D) with the tile's LSE and D read
-// from shared memory (every lane reads the same word: a broadcast); P^T over S^T
-// and dS^T over dP^T in bf16.  At the end of the unit dV and dK = scale * (...) in bf16.
-template <int D>
-__device__ __forceinline__ void bwd_dkdv_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem,
-                                              float* vec) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int r = warp * 32 + lane;
-  const uint32_t lane_off = uint32_t(warp * 32) << 16;
-  const uint32_t t_s = tmem + lane_off + COL_S, t_dp = tmem + lane_off + COL_DP, t_acc = tmem + lane_off + COL_ACC;
-  const float sl2 = p.scale_log2;
-  const int G = gridDim.x;
-  uint32_t sf = 0, of = 0;
-  int it = 0;  // steps so far: picks the vector buffer and its barrier phase
-  bool ok = true;
-  for (int k = 0; ok && k * G < p.num_units; ++k) {
-    const int w = bwd_unit_of(k, blockIdx.x, G);
-    if (w >= p.num_units) continue;
-    int bh, rt, first, n;
-    bwd_decode<1>(p, w, bh, rt, first, n);
-    const int k0 = rt * BT, key = k0 + r;
+    const float lse2_row = (KIND == 0 && row < p.T) ? p.lse[ri] * LOG2E : 0.f;
+    const float d_row = (KIND == 0 && row < p.T) ? p.drow[ri] : 0.f;
     for (int t = 0; t < n; ++t, ++it) {
-      const int q0 = (first + t) * BT;
-      float* lv = vec + (it & 1) * 2 * BT;  // [0, 128): LSE * log2 e; [128, 256): D
-      {
-        const int q = q0 + r;
+      const int c0 = (first + t) * BT;  // first column of the step: a key (KIND 0) or query (KIND 1)
+      const float* lv = vec + (it & 1) * 2 * BT + HC * h;  // KIND 1: this half's LSE * log2 e; + BT: D
+      if (KIND == 1) {  // half 0 writes the tile's LSE * log2 e, half 1 its D
+        const int q = c0 + r;
         const size_t qi = static_cast<size_t>(bh) * p.T + q;
-        lv[r] = q < p.T ? p.lse[qi] * LOG2E : INFINITY;  // rows past T: P = 0
-        lv[BT + r] = q < p.T ? p.drow[qi] : 0.f;
+        float* lw = vec + (it & 1) * 2 * BT + h * BT;
+        lw[r] = h == 0 ? (q < p.T ? p.lse[qi] * LOG2E : INFINITY)  // queries past T: P = 0
+                       : (q < p.T ? p.drow[qi] : 0.f);
         mbar_arrive(B.vec_full + 8 * (it & 1));
+        if (!(ok = W.wait(B.vec_full + 8 * (it & 1), (it >> 1) & 1))) break;
       }
-      if (!(ok = W.wait(B.vec_full + 8 * (it & 1), (it >> 1) & 1))) break;
+      // columns valid for this row: KIND 0 keys < min(T, row + 1) (causal); KIND 1 queries >= row
+      int lim = BT, lo = 0;
+      if (KIND == 0) {
+        if ((p.causal && c0 + BT - 1 > r0) || c0 + BT > p.T) {
+          lim = p.T - c0;
+          if (p.causal) lim = min(lim, row - c0 + 1);
+        }
+      } else if (p.causal && c0 == r0) {
+        lo = r;  // the diagonal tile: query q sees key `row` only if q >= row
+      }
+      lim -= HC * h;  // in this half's column numbering
+      lo -= HC * h;
       if (!(ok = W.wait(B.s_full, sf))) break;
       sf ^= 1;
       tc_fence_after();
-      const bool diag = p.causal && q0 == k0;  // query q sees this key only if q >= key
+      uint32_t pp[HC / 2];  // P as bf16 pairs
 #pragma unroll
-      for (int c = 0; c < BT / 32; ++c) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32x2_wait(t_s + 32 * c, sv, t_dp + 32 * c, dv);
-        uint32_t pp[16], pd[16];
+      for (int c = 0; c < HC / 32; ++c) {
+        uint32_t sv[32];
+        tmem_ld32_wait(t_s + 32 * c, sv);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int c0 = 32 * c + 2 * e;
-          const float2 l2 = *reinterpret_cast<const float2*>(lv + c0);
-          const float2 dd = *reinterpret_cast<const float2*>(lv + BT + c0);
-          float p0 = ex2_approx(fmaf(u2f(sv[2 * e]), sl2, -l2.x));
-          float p1 = ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, -l2.y));
-          if (diag && c0 < r) p0 = 0.f;
-          if (diag && c0 + 1 < r) p1 = 0.f;
-          pp[e] = pack_bf16x2(p0, p1);
-          pd[e] = pack_bf16x2(p0 * (u2f(dv[2 * e]) - dd.x), p1 * (u2f(dv[2 * e + 1]) - dd.y));
+          const int cc = 32 * c + 2 * e;
+          float l0 = lse2_row, l1 = lse2_row;
+          if (KIND == 1) {
+            const float2 l2 = *reinterpret_cast<const float2*>(lv + cc);
+            l0 = l2.x;
+            l1 = l2.y;
+          }
+          float p0 = ex2_approx(fmaf(u2f(sv[2 * e]), sl2, -l0));
+          float p1 = ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, -l1));
+          if (cc >= lim || cc < lo) p0 = 0.f;
+          if (cc + 1 >= lim || cc + 1 < lo) p1 = 0.f;
+          pp[16 * c + e] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(t_s + 16 * c, pp);
-        tmem_st16(t_dp + 16 * c, pd);
+      }
+      if (SC::SPLIT) {  // S may now be overwritten by the next step's; P / dS wait for the previous products
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.s_free);
+        if (it > 0) {
+          if (!(ok = W.wait(B.pv_done, pvd))) break;
+          pvd ^= 1;
+          tc_fence_after();
+        }
+      }
+      if (KIND == 1) {
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c)
+          tmem_st16(t_p + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pp + 16 * c));
+      }
+      if (SC::SPLIT) {
+        if (!(ok = W.wait(B.dp_full, dpf))) break;
+        dpf ^= 1;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < HC / 32; ++c) {  // dS, 32 columns at a time (in place over dP without SPLIT)
+        uint32_t dv[32];
+        tmem_ld32_wait(t_dp + 32 * c, dv);
+        uint32_t pd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int cc = 32 * c + 2 * e;
+          float d0 = d_row, d1 = d_row;
+          if (KIND == 1) {
+            const float2 dd = *reinterpret_cast<const float2*>(lv + BT + cc);
+            d0 = dd.x;
+            d1 = dd.y;
+          }
+          const uint32_t pw = pp[16 * c + e];
+          pd[e] = pack_bf16x2(u2f(pw << 16) * (u2f(dv[2 * e]) - d0), u2f(pw & 0xFFFF0000u) * (u2f(dv[2 * e + 1]) - d1));
+        }
+        tmem_st16(t_ds + 16 * c, pd);
+      }
+      if (SC::SPLIT) {  // dP may now be overwritten by the next step's
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.dp_free);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -476,20 +556,20 @@ __device__ __forceinline__ void bwd_dkdv_rows(const BwdParams& p, const Waiter& 
     if (!(ok = W.wait(B.o_full, of))) break;
     of ^= 1;
     tc_fence_after();
-    const size_t ki = static_cast<size_t>(bh) * p.T + key;
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {  // 0: dV, 1: dK (times scale)
-      __nv_bfloat16* out = (part ? p.dk : p.dv) + ki * D;
-      const float f = part ? p.scale : 1.f;
+    for (int part = 0; part < (KIND == 0 ? 1 : 2); ++part) {  // KIND 0: dQ; KIND 1: dV, then dK
+      __nv_bfloat16* out = (KIND == 0 ? p.dq : (part ? p.dk : p.dv)) + ri * D;
+      const float f = (KIND == 0 || part) ? p.scale : 1.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {  // this half's columns of the accumulator
+        const int col = h * (D / 2) + 32 * c;
         uint32_t v[32];
-        tmem_ld32_wait(t_acc + part * D + 32 * c, v);
+        tmem_ld32_wait(t_acc + part * D + col, v);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * f, u2f(v[2 * e + 1]) * f);
-        if (key < p.T) {
-          uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+        if (row < p.T) {
+          uint4* dst = reinterpret_cast<uint4*>(out + col);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
@@ -528,10 +608,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     bwd_mma<D, KIND>(p, W, B, sbase, tmem);
     __syncwarp();
   } else {
-    if (KIND == 0)
-      bwd_dq_rows<D>(p, W, B, tmem);
-    else
-      bwd_dkdv_rows<D>(p, W, B, tmem, reinterpret_cast<float*>(smem + L::VEC_OFF));
+    bwd_rows<D, KIND>(p, W, B, tmem, reinterpret_cast<float*>(smem + L::VEC_OFF));
   }
   bwd_teardown<D>(tmem, warp);
 }
