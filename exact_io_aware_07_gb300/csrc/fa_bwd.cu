@@ -333,7 +333,17 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
     ++nu;
     tc_fence_after();
     int s0 = 0, s1 = 0;  // ring stages of the current step's two streamed tiles
-    if (SC::SPLIT) {
+    if (!SC::SPLIT) {
+      do {  // step 0's two products
+        BWD_TAKE(s0);
+        BWD_SCORE(COL_S, 0, s0);
+        mma_commit_elect(B.s_full);
+        BWD_TAKE(s1);
+        BWD_SCORE(COL_DP, 1, s1);
+        mma_commit_elect(B.dp_full);
+      } while (0);
+      if (!ok) break;
+    } else {
       do {  // step 0's two products
         BWD_TAKE(s0);
         {
@@ -356,13 +366,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
     }
     for (int t = 0; t < n; ++t) {
       int n0 = -1, n1 = -1;
-      if (!SC::SPLIT) {
-        BWD_TAKE(s0);
-        BWD_TAKE(s1);
-        BWD_SCORE(COL_S, 0, s0);
-        BWD_SCORE(COL_DP, 1, s1);
-        mma_commit_elect(B.s_full);
-      } else if (t + 1 < n) {  // the next step's products, as soon as this step's have been read
+      if (SC::SPLIT && t + 1 < n) {  // the next step's products, as soon as this step's have been read
         BWD_TAKE(n0);
         {
           uint32_t par = sfr ^ 1;
@@ -389,21 +393,35 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
       const uint32_t acc0 = t > 0 ? 1u : 0u;
       if (KIND == 0) {
         BWD_GRAD(COL_ACC, SC::COL_DS, s0, acc0);  // dQ += dS K_j
-      } else {
+      } else if (SC::SPLIT) {
         BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);       // dV += P^T dO_i
+        BWD_GRAD(COL_ACC + D, SC::COL_DS, s0, acc0);  // dK += dS^T Q_i
+      } else {
+        // P^T and dS^T sit over S^T and dP^T: the next step's S^T follows dV (which reads
+        // P^T) and its dP^T follows dK (which reads dS^T), so the row warps can start on the
+        // next S^T while dK and the next dP^T run
+        BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);  // dV += P^T dO_i
+        if (t + 1 < n) {
+          BWD_TAKE(n0);
+          BWD_SCORE(COL_S, 0, n0);
+          mma_commit_elect(B.s_full);
+        }
         BWD_GRAD(COL_ACC + D, SC::COL_DS, s0, acc0);  // dK += dS^T Q_i
       }
       if (SC::SPLIT) mma_commit_elect(B.pv_done);
       mma_commit_elect(B.ring_empty + 8 * s0);
       mma_commit_elect(B.ring_empty + 8 * s1);
+      if (!SC::SPLIT && t + 1 < n) {
+        BWD_TAKE(n1);
+        BWD_SCORE(COL_DP, 1, n1);
+        mma_commit_elect(B.dp_full);
+      }
       if (t + 1 == n) {
         mma_commit_elect(B.res_empty);
         mma_commit_elect(B.o_full);
       }
-      if (SC::SPLIT) {
-        s0 = n0;
-        s1 = n1;
-      }
+      s0 = n0;
+      s1 = n1;
     }
   }
 #undef BWD_TAKE
@@ -502,11 +520,11 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
           pp[16 * c + e] = pack_bf16x2(p0, p1);
         }
       }
-      if (SC::SPLIT) {  // S may now be overwritten by the next step's; P / dS wait for the previous products
+      if (SC::SPLIT) {  // S may now be overwritten by the next step's; P waits for the previous products
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(B.s_free);
-        if (it > 0) {
+        if (KIND == 1 && it > 0) {
           if (!(ok = W.wait(B.pv_done, pvd))) break;
           pvd ^= 1;
           tc_fence_after();
@@ -517,13 +535,15 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
         for (int c = 0; c < HC / 32; ++c)
           tmem_st16(t_p + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pp + 16 * c));
       }
-      if (SC::SPLIT) {
-        if (!(ok = W.wait(B.dp_full, dpf))) break;
-        dpf ^= 1;
-        tc_fence_after();
-      }
+      if (!(ok = W.wait(B.dp_full, dpf))) break;
+      dpf ^= 1;
+      tc_fence_after();
+      // dS, 32 columns at a time: stored as it is formed (in place over dP without SPLIT, or into
+      // the dS^T columns once the previous step's products are done), or, in the dQ kernel, kept
+      // until dP is released and the previous dQ product has read the dS columns
+      uint32_t pdk[KIND == 0 ? HC / 2 : 1];
 #pragma unroll
-      for (int c = 0; c < HC / 32; ++c) {  // dS, 32 columns at a time (in place over dP without SPLIT)
+      for (int c = 0; c < HC / 32; ++c) {
         uint32_t dv[32];
         tmem_ld32_wait(t_dp + 32 * c, dv);
         uint32_t pd[16];
@@ -538,14 +558,24 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
           }
           const uint32_t pw = pp[16 * c + e];
           pd[e] = pack_bf16x2(u2f(pw << 16) * (u2f(dv[2 * e]) - d0), u2f(pw & 0xFFFF0000u) * (u2f(dv[2 * e + 1]) - d1));
+          if (KIND == 0) pdk[16 * c + e] = pd[e];
         }
-        tmem_st16(t_ds + 16 * c, pd);
+        if (KIND == 1) tmem_st16(t_ds + 16 * c, pd);
       }
       if (SC::SPLIT) {  // dP may now be overwritten by the next step's
-        tmem_wait_st();
+        if (KIND == 1) tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(B.dp_free);
+      }
+      if (KIND == 0) {  // the previous dQ product has read the dS columns: store this step's
+        if (it > 0) {
+          if (!(ok = W.wait(B.pv_done, pvd))) break;
+          pvd ^= 1;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c) tmem_st16(t_ds + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pdk + 16 * c));
       }
       tmem_wait_st();
       tc_fence_before();
