@@ -131,16 +131,17 @@ fa_status validate_host(const void* q, const void* k, const void* v, const void*
 }
 
 // 3-D view (inner, rows, B*H) of a contiguous tensor: a box (128 bytes of the inner
-// dimension x 128 rows x 1) never crosses from one head into the next, and rows past
-// `rows` read as zeros.  bf16 (d, T, B*H) views, or byte views for e4m3 tensors.
-bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int rows, int inner, bool bytes) {
+// dimension x box_rows rows x 1) never crosses from one head into the next, rows past
+// `rows` read as zeros and are not written.  bf16 (d, T, B*H) views, or byte views for
+// e4m3 tensors.
+bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int rows, int inner, bool bytes, int box_rows) {
   const DriverFns& fns = driver_fns();
   if (!fns.encode_tiled) return false;
   const cuuint64_t es = bytes ? 1 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * es, static_cast<cuuint64_t>(rows) * inner * es};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 128, 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   return fns.encode_tiled(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -152,7 +153,7 @@ bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int rows, int
 // memory, so a cached descriptor is exactly what encoding again would give).
 struct MapCacheEntry {
   const void* base = nullptr;
-  int BH = 0, T = 0, d = 0;
+  int BH = 0, T = 0, d = 0, box_rows = 0;
   bool bytes = false;
   CUtensorMap map;
 };
@@ -160,19 +161,21 @@ constexpr int kMapCache = 16;
 MapCacheEntry g_map_cache[kMapCache];
 std::mutex g_map_mu;
 
-bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d, bool bytes = false) {
-  const size_t slot = (reinterpret_cast<uintptr_t>(base) >> 8) % kMapCache;
+bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d, bool bytes = false,
+                     int box_rows = 128) {
+  const size_t slot = ((reinterpret_cast<uintptr_t>(base) >> 8) + (box_rows == 128 ? 0 : 1)) % kMapCache;
   std::lock_guard<std::mutex> lock(g_map_mu);
   MapCacheEntry& e = g_map_cache[slot];
-  if (e.base == base && e.BH == BH && e.T == T && e.d == d && e.bytes == bytes) {
+  if (e.base == base && e.BH == BH && e.T == T && e.d == d && e.bytes == bytes && e.box_rows == box_rows) {
     *map = e.map;
     return true;
   }
-  if (!encode_tensor_map(map, base, BH, T, d, bytes)) return false;
+  if (!encode_tensor_map(map, base, BH, T, d, bytes, box_rows)) return false;
   e.base = base;
   e.BH = BH;
   e.T = T;
   e.d = d;
+  e.box_rows = box_rows;
   e.bytes = bytes;
   e.map = *map;
   return true;
@@ -180,7 +183,7 @@ bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d, b
 
 struct Prepared {
   fa::Params p{};
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;  // to: the bf16 output O, written in boxes of 32 rows
   int dev = 0, num_sms = 0;
 };
 
@@ -211,7 +214,7 @@ fa_status prepare(const void* q, const void* k, const void* v, void* o, float* l
     if (overlaps(o, q_bytes, in.p, in.n) || overlaps(lse, lse_bytes, in.p, in.n)) return FA_ERR_ALIAS;
   if (overlaps(o, q_bytes, lse, lse_bytes)) return FA_ERR_ALIAS;
   if (!make_tensor_map(&pr->tq, q, BH, T, d) || !make_tensor_map(&pr->tk, k, BHkv, T, d) ||
-      !make_tensor_map(&pr->tv, v, BHkv, T, d))
+      !make_tensor_map(&pr->tv, v, BHkv, T, d) || !make_tensor_map(&pr->to, o, BH, T, d, false, fa::kOutBoxRows))
     return FA_ERR_CUDA;
   fa::Params& p = pr->p;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -273,7 +276,7 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
   fa_status st = prepare(q, k, v, o, lse, B, H, Hkv, T, d, causal, scale, &pr);
   if (st != FA_OK) return st;
   const int grid = pr.p.num_units < pr.num_sms ? pr.p.num_units : pr.num_sms;
-  if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, pr.p, grid, stream) != cudaSuccess) {
+  if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, pr.to, pr.p, grid, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
@@ -315,7 +318,8 @@ fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, 
   pr.num_sms = num_sms;
   // page pools as (d, 128 rows, num_pages * Hkv): one TMA box is one page of one head
   if (!make_tensor_map(&pr.tq, q, BH, T, d) || !make_tensor_map(&pr.tk, k_pages, num_pages * Hkv, 128, d) ||
-      !make_tensor_map(&pr.tv, v_pages, num_pages * Hkv, 128, d))
+      !make_tensor_map(&pr.tv, v_pages, num_pages * Hkv, 128, d) ||
+      !make_tensor_map(&pr.to, o, BH, T, d, false, fa::kOutBoxRows))
     return FA_ERR_CUDA;
   fa::Params& p = pr.p;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -338,7 +342,7 @@ fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, 
   p.num_splits = 1;
   p.split_tiles = p.nk;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-  if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, p, grid, stream) != cudaSuccess) {
+  if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, pr.to, p, grid, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
@@ -425,9 +429,10 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
     for (int b = a + 1; b < 3; ++b)
       if (overlaps(outs[a].p, outs[a].n, outs[b].p, outs[b].n)) return FA_ERR_ALIAS;
   }
-  CUtensorMap tq, tk, tvt;
+  CUtensorMap tq, tk, tvt, to;
   if (!make_tensor_map(&tq, q, BH, T, 128, true) || !make_tensor_map(&tk, k, BH, T, 128, true) ||
-      !make_tensor_map(&tvt, workspace, BH, 128, Tp, true))
+      !make_tensor_map(&tvt, workspace, BH, 128, Tp, true) ||
+      !make_tensor_map(&to, o, BH, T, 128, false, fa::kOutBoxRows))
     return FA_ERR_CUDA;
   fa::Params p{};
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -449,7 +454,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
   p.split_tiles = p.nk;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   if (fa::launch_transpose_e4m3(v, workspace, BH, T, Tp, stream) != cudaSuccess ||
-      fa::launch_fa_fwd_e4m3(tq, tk, tvt, p, grid, stream) != cudaSuccess) {
+      fa::launch_fa_fwd_e4m3(tq, tk, tvt, to, p, grid, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }

@@ -219,13 +219,6 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
                                              const CUtensorMap* mapA, const CUtensorMap* mapB,
                                              const CUtensorMap* mapC, const CUtensorMap* mapD) {
   using L = BwdLayout<D>;
-  const int lane = threadIdx.x % 32;
-  if (lane == 0) {
-    tma_prefetch_desc(mapA);
-    tma_prefetch_desc(mapB);
-    tma_prefetch_desc(mapC);
-    tma_prefetch_desc(mapD);
-  }
   const int G = gridDim.x;
   int stage = 0, nu = 0;
   uint32_t phase = 0, issued = 0, issued_parity = 0;
@@ -625,7 +618,14 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int warp = threadIdx.x / 32;
   const uint32_t tmem = bwd_setup<D>(smem, B, tmem_slot, abort_flag, warp);
   const Waiter W{abort_flag, p.timeout_ns, &g_bwd_status};
-  // the set-up above overlaps the previous kernel's tail; memory is read only after it has finished
+  // the set-up above overlaps the previous kernel's tail; memory is read only after it has
+  // finished (the tensor maps are kernel parameters, so fetching them may start earlier)
+  if (warp == BWD_PRODUCER && threadIdx.x % 32 == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
   pdl_launch_dependents();
   pdl_wait();
   if (warp == BWD_PRODUCER) {

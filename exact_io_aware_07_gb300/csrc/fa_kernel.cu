@@ -23,7 +23,8 @@
 //
 // Roles (one CTA per SM, persistent over work units):
 //   warps 0-3  softmax for query tile 0 of the unit (one TMEM lane = one row per thread)
-//   warps 4-7  softmax for query tile 1
+//   warps 4-7  softmax for query tile 1 (d = 64: the tiles of a causal unit may be handed
+//              to the two slots the other way round, see balance_slots)
 //   warp 8     TMA producer: Q tiles once per unit, then K_j, V_j through a ring
 //   warp 9     Tensor Memory allocator; tcgen05.mma issuer (d = 128: both tiles;
 //              d = 64: tile 0)
@@ -82,7 +83,10 @@ struct Layout {
   // d = 64: one MMA-issuing warp per query tile (warps 9, 10; warp 11 idle); d = 128: warp 9 alone
   static constexpr int THREADS = SEP_P ? 384 : 320;
   static constexpr int MMA_WARPS = SEP_P ? 2 : 1;
-  static constexpr int BAR_OFF = KV_OFF + STAGES * TILE_BYTES;
+  // bf16 O staging: 32 rows x 64 columns (4 KB, 128-byte swizzle) per softmax warp
+  static constexpr int STG_OFF = KV_OFF + STAGES * TILE_BYTES;
+  static constexpr int STG_WARP_BYTES = 32 * 128;
+  static constexpr int BAR_OFF = STG_OFF + 8 * STG_WARP_BYTES;
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2],
   // s_free[2], done
   static constexpr int NUM_BARS = 4 + 2 * STAGES + 10 + 1;
@@ -104,7 +108,8 @@ static_assert(Layout<64>::SMEM_BYTES <= MAX_SMEM_PER_CTA && Layout<128>::SMEM_BY
 struct Unit {
   int bh, qb;
   int jb;      // first K/V tile of the unit (0 unless the key range is split)
-  int n0, n1;  // K/V tiles each query tile visits from jb (0 = nothing to do for that tile)
+  int n0, n1;  // K/V tiles slot 0 / slot 1 visits from jb (0 = nothing to do for that slot)
+  int sw;      // slot i holds query tile i ^ sw of the unit (see balance_slots)
 };
 
 // Work item w -> (batch*head, 256-row query block[, key split]).  Causal
@@ -129,6 +134,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
   const int q0 = u.qb * 2 * BM, q1 = q0 + BM;
   const int e0 = (q0 >= p.T) ? 0 : (p.causal ? min(p.nk, q0 / BN + 1) : p.nk);  // tiles visible to tile 0
   const int e1 = (q1 >= p.T) ? 0 : (p.causal ? min(p.nk, q1 / BN + 1) : p.nk);
+  u.sw = 0;
   if (PARTIAL) {
     u.jb = s * p.split_tiles;
     const int end = u.jb + p.split_tiles;
@@ -142,6 +148,20 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
   return u;
 }
 
+// d = 64, where each query tile has an MMA warp and a softmax warpgroup of its own: the two
+// tiles of a causal unit see different numbers of K/V tiles, so the longer one goes to the
+// slot that has had less work so far in this CTA (bal = K/V steps of slot 0 minus slot 1).
+// Every role walks the same list of units and reaches the same assignment.
+__device__ __forceinline__ void balance_slots(Unit& u, int& bal) {
+  if (u.n0 != u.n1 && bal != 0 && ((u.n1 > u.n0) == (bal < 0))) {
+    const int t = u.n0;
+    u.n0 = u.n1;
+    u.n1 = t;
+    u.sw = 1;
+  }
+  bal += u.n0 - u.n1;
+}
+
 // The k-th work item of CTA b in a grid of G: a snake over the heavy-first list
 // (b, 2G-1-b, 2G+b, ...), which pairs long causal units with short ones.
 __device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k & 1) ? (G - 1 - b) : b); }
@@ -152,7 +172,7 @@ __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 template <int D, bool PARTIAL, bool F8 = false>
 __global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const Params p) {
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Params p) {
   using L = Layout<D, F8>;
   static_assert(!F8 || (D == 128 && !PARTIAL), "the e4m3 path is d = 128, unsplit");
   extern __shared__ uint8_t smem_raw[];
@@ -209,27 +229,31 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.timeout_ns, &g_status};
-  // the set-up above overlaps the previous kernel's tail; inputs are read only after it has finished
+  // the set-up above overlaps the previous kernel's tail; inputs are read only after it has
+  // finished (the tensor maps are kernel parameters, so fetching them may start earlier)
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (!PARTIAL && warp == 0 && lane == 0) tma_prefetch_desc(&tmO);
   pdl_launch_dependents();
   pdl_wait();
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer (whole warp, one lane issues)
     {
-      if (lane == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0, q_issued = 0, q_parity = 0;  // for draining after a timeout
       bool ok = true;
       int nu = 0;  // units this CTA has started
+      int bal = 0;
       for (int k = 0; ok && k * G < p.num_units; ++k) {
         const int w = unit_of(k, blockIdx.x, G);
         if (w >= p.num_units) continue;
-        const Unit u = decode_unit<PARTIAL>(p, w);
+        Unit u = decode_unit<PARTIAL>(p, w);
+        if (L::SEP_P) balance_slots(u, bal);
         const int nmax = max(u.n0, u.n1);
         if (nmax == 0) continue;  // an empty key split: no role touches it
         // the K/V head this query head reads (query heads share K/V heads in groups)
@@ -246,7 +270,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
           for (int b = 0; b < L::BOXES; ++b)
             tma_load_3d_elect(q_smem + (2 * qb + i) * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64,
-                        u.qb * 2 * BM + i * BM, u.bh, bar_q_full + 8 * qb);
+                        u.qb * 2 * BM + (i ^ u.sw) * BM, u.bh, bar_q_full + 8 * qb);
         }
         q_issued |= 1u << qb;
         q_parity = (q_parity & ~(1u << qb)) | (qpar << qb);
@@ -340,10 +364,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       uint32_t pf = 0, oe = 0, sfr = 0;
       bool ok = true;
       int nu = 0;
+      int bal = 0;
       for (int k = 0; ok && k * G < p.num_units; ++k) {
         const int w = unit_of(k, blockIdx.x, G);
         if (w >= p.num_units) continue;
-        const Unit u = decode_unit<PARTIAL>(p, w);
+        Unit u = decode_unit<PARTIAL>(p, w);
+        balance_slots(u, bal);
         const int n = i ? u.n1 : u.n0, nmax = max(u.n0, u.n1);
         if (nmax == 0) continue;
         const int qb = nu % L::QBUF;
@@ -599,15 +625,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t my_s_full = bar_s_full + 8 * i, my_p_full = bar_p_full + 8 * i, my_s_free = bar_s_free + 8 * i;
     const uint32_t my_o_full = bar_o_full + 8 * i, my_o_empty = bar_o_empty + 8 * i;
     const float sl2 = p.scale_log2;
+    const uint32_t stg = sbase + L::STG_OFF + warp * L::STG_WARP_BYTES;  // this warp's O staging
+    bool stg_busy = false;  // a TMA store from the staging buffer may still be reading it
     uint32_t sf_phase = 0, of_phase = 0;
     bool ok = true;
+    int bal = 0;
     for (int k = 0; ok && k * G < p.num_units; ++k) {
       const int w = unit_of(k, blockIdx.x, G);
       if (w >= p.num_units) continue;
-      const Unit u = decode_unit<PARTIAL>(p, w);
+      Unit u = decode_unit<PARTIAL>(p, w);
+      if (L::SEP_P) balance_slots(u, bal);
       const int n = i ? u.n1 : u.n0;
       if (n == 0) continue;
-      const int q0 = u.qb * 2 * BM + i * BM;
+      const int q0 = u.qb * 2 * BM + (i ^ u.sw) * BM;
       const int row = q0 + rt;
       float m_run = -INFINITY;  // reference max, base-2 units of the scaled score
       float l = 0.f;            // sum of the fp32 weights: the softmax denominator of the LSE
@@ -684,11 +714,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               continue;
             }
             pk[16 * c + e] = pack_bf16x2(p0, p1);
-            // sum of the bf16 weights (the two forms measure fastest at d = 64 and d = 128)
-            if (L::SEP_P)  // bf16 -> fp32 is a shift / mask of the packed word, then one packed add
-              fadd2(lr0, lr1, u2f(pk[16 * c + e] << 16), u2f(pk[16 * c + e] & 0xFFFF0000u));
-            else
-              add_bf16x2_f32(pk[16 * c + e], lr0, lr1);
+            add_bf16x2_f32(pk[16 * c + e], lr0, lr1);  // sum of the bf16 weights
           }
           if (F8) {
             float h0, h1;
@@ -750,26 +776,47 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         if (row < p.T) p.lsepart[prow] = (m_run + log2f(l)) * LN2;
       } else {
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(u.bh) * p.T + row) * D;
+        // O in bf16 through shared memory: the warp's 32 rows x 64 columns in the 128-byte
+        // swizzled layout of the output map (16-byte chunk c of row r at chunk c ^ (r % 8), so
+        // every group of eight lanes hits eight different banks), then one TMA store per 64
+        // columns.  Rows past T lie outside the map and are not written.
+        const int y0 = q0 + wq * 32;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32_wait(t_o + c * 32, ov);
-        uint32_t pk[16];
+        for (int h = 0; h < D / 64; ++h) {
+          if (stg_busy) {  // the previous box must have been read out of the staging buffer
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+          }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(ov[2 * e]) * inv_l, u2f(ov[2 * e + 1]) * inv_l);
-        if (row < p.T) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t ov[32];
+            tmem_ld32_wait(t_o + h * 64 + c2 * 32, ov);
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(ov[2 * e]) * inv_l, u2f(ov[2 * e + 1]) * inv_l);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(stg + lane * 128 + ((uint32_t(c2 * 4 + q) ^ uint32_t(lane & 7)) << 4), pk[4 * q],
+                           pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (y0 < p.T) {
+            if (lane == 0) {
+              tma_store_3d(&tmO, stg, h * 64, y0, u.bh);
+              bulk_commit_group();
+            }
+            stg_busy = true;
+          }
         }
-      }
-      if (row < p.T) p.lse[static_cast<size_t>(u.bh) * p.T + row] = (m_run + log2f(l)) * LN2;
+        if (row < p.T) p.lse[static_cast<size_t>(u.bh) * p.T + row] = (m_run + log2f(l)) * LN2;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(my_o_empty);
     }
+    if (stg_busy && lane == 0) bulk_wait_group0();  // this warp's O stores have completed
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -799,8 +846,8 @@ __global__ void fa_wait_selftest_kernel(unsigned long long timeout_ns) {
 // ---------------------------------------------------------------- host side
 
 template <int D, bool PARTIAL, bool F8 = false>
-static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
-                          int grid, cudaStream_t stream) {
+static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                          const Params& p, int grid, cudaStream_t stream) {
   using L = Layout<D, F8>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -822,14 +869,14 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL, F8>, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL, F8>, q, k, v, o, p);
 }
 
 static_assert(Layout<128, true>::SMEM_BYTES <= MAX_SMEM_PER_CTA, "e4m3 layout exceeds the per-CTA limit");
 
-cudaError_t launch_fa_fwd_e4m3(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt, const Params& p,
-                               int grid, cudaStream_t stream) {
-  return launch<128, false, true>(q, k, vt, p, grid, stream);
+cudaError_t launch_fa_fwd_e4m3(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt,
+                               const CUtensorMap& o, const Params& p, int grid, cudaStream_t stream) {
+  return launch<128, false, true>(q, k, vt, o, p, grid, stream);
 }
 
 int fa_fwd_e4m3_smem_bytes() { return Layout<128, true>::SMEM_BYTES; }
@@ -874,15 +921,16 @@ cudaError_t launch_transpose_e4m3(const void* v, void* vt, int BH, int T, int Tp
 }
 
 cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const Params& p, int grid, cudaStream_t stream) {
-  if (d == 64) return launch<64, false>(q, k, v, p, grid, stream);
-  return launch<128, false>(q, k, v, p, grid, stream);
+                          const CUtensorMap& o, const Params& p, int grid, cudaStream_t stream) {
+  if (d == 64) return launch<64, false>(q, k, v, o, p, grid, stream);
+  return launch<128, false>(q, k, v, o, p, grid, stream);
 }
 
+// (the partial form writes fp32 rows directly and never uses the output map; q stands in for it)
 cudaError_t launch_fa_fwd_partial(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                   const Params& p, int grid, cudaStream_t stream) {
-  if (d == 64) return launch<64, true>(q, k, v, p, grid, stream);
-  return launch<128, true>(q, k, v, p, grid, stream);
+  if (d == 64) return launch<64, true>(q, k, v, q, p, grid, stream);
+  return launch<128, true>(q, k, v, q, p, grid, stream);
 }
 
 // Merge of the per-split partials of every row ("FlashAttention and Fused

@@ -34,11 +34,14 @@ struct Params {
   float* lsepart;             // [num_splits][BH*T] fp32 partial LSE (natural log)
 };
 
+// Rows per box of the output tensor map `o` (bf16 (d, T, B*H), 128-byte swizzle): each
+// softmax warp writes its 32 rows of a query tile with one TMA store per 64 columns.
+constexpr int kOutBoxRows = 32;
 cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const Params& p, int grid, cudaStream_t stream);
-// e4m3 Q, K and a transposed e4m3 V ((B*H, d, Tp) bytes), d = 128.
-cudaError_t launch_fa_fwd_e4m3(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt, const Params& p,
-                               int grid, cudaStream_t stream);
+                          const CUtensorMap& o, const Params& p, int grid, cudaStream_t stream);
+// e4m3 Q, K and a transposed e4m3 V ((B*H, d, Tp) bytes), d = 128; bf16 O as above.
+cudaError_t launch_fa_fwd_e4m3(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt,
+                               const CUtensorMap& o, const Params& p, int grid, cudaStream_t stream);
 // V (B*H, T, 128) e4m3 -> V^T (B*H, 128, Tp) with keys Tp > T zero (Tp = T rounded up to 16).
 cudaError_t launch_transpose_e4m3(const void* v, void* vt, int BH, int T, int Tp, cudaStream_t stream);
 int fa_fwd_e4m3_smem_bytes();
