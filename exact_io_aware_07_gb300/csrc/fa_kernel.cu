@@ -73,7 +73,7 @@ struct Layout {
   // d = 64 and e4m3: two units' Q tiles resident (the next unit's load overlaps the
   // current unit); bf16 d = 128: one unit's Q tiles, the next unit's prefetched into L2.
   static constexpr int QBUF = (D == 128 && !F8) ? 1 : 2;
-  static constexpr int STAGES = F8 ? 8 : (D == 128) ? 4 : 6;   // K/V ring depth (tiles)
+  static constexpr int STAGES = (D == 128 && !F8) ? 4 : 6;     // K/V ring depth (tiles)
   static constexpr int Q_OFF = 0;                      // [QBUF units][2 query tiles]
   static constexpr int KV_OFF = QBUF * 2 * TILE_BYTES;
   // d = 64: P_i has Tensor Memory columns of its own, so S_i(j+1) may be computed
@@ -83,9 +83,12 @@ struct Layout {
   // d = 64: one MMA-issuing warp per query tile (warps 9, 10; warp 11 idle); d = 128: warp 9 alone
   static constexpr int THREADS = SEP_P ? 384 : 320;
   static constexpr int MMA_WARPS = SEP_P ? 2 : 1;
-  // bf16 O staging: 32 rows x 64 columns (4 KB, 128-byte swizzle) per softmax warp
+  // bf16 O staging per softmax warp: 32 rows x 64 columns (4 KB, 128-byte swizzle), and for
+  // e4m3 (d = 128, where the ring's tiles are half as large) a second one, so that the two
+  // 64-column halves of a row need not wait for each other's store
   static constexpr int STG_OFF = KV_OFF + STAGES * TILE_BYTES;
-  static constexpr int STG_WARP_BYTES = 32 * 128;
+  static constexpr bool STG2 = F8;
+  static constexpr int STG_WARP_BYTES = (STG2 ? 2 : 1) * 32 * 128;
   static constexpr int BAR_OFF = STG_OFF + 8 * STG_WARP_BYTES;
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2],
   // s_free[2], done
@@ -783,27 +786,31 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int y0 = q0 + wq * 32;
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          if (stg_busy) {  // the previous box must have been read out of the staging buffer
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
-          }
+          uint32_t pk[2][16];
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             uint32_t ov[32];
             tmem_ld32_wait(t_o + h * 64 + c2 * 32, ov);
-            uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(ov[2 * e]) * inv_l, u2f(ov[2 * e + 1]) * inv_l);
+            for (int e = 0; e < 16; ++e)
+              pk[c2][e] = pack_bf16x2(u2f(ov[2 * e]) * inv_l, u2f(ov[2 * e + 1]) * inv_l);
+          }
+          const uint32_t buf = stg + (L::STG2 ? h * 32 * 128 : 0);
+          if (stg_busy && (!L::STG2 || h == 0)) {  // earlier boxes must have been read out of it
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              st_shared_v4(stg + lane * 128 + ((uint32_t(c2 * 4 + q) ^ uint32_t(lane & 7)) << 4), pk[4 * q],
-                           pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
+              st_shared_v4(buf + lane * 128 + ((uint32_t(c2 * 4 + q) ^ uint32_t(lane & 7)) << 4), pk[c2][4 * q],
+                           pk[c2][4 * q + 1], pk[c2][4 * q + 2], pk[c2][4 * q + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (y0 < p.T) {
             if (lane == 0) {
-              tma_store_3d(&tmO, stg, h * 64, y0, u.bh);
+              tma_store_3d(&tmO, buf, h * 64, y0, u.bh);
               bulk_commit_group();
             }
             stg_busy = true;
