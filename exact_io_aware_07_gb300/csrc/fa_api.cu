@@ -130,22 +130,24 @@ fa_status validate_host(const void* q, const void* k, const void* v, const void*
   return FA_OK;
 }
 
-// 3-D view (inner, rows, B*H) of a contiguous tensor: a box (128 bytes of the inner
+// 3-D view (inner, rows, B*H) of a contiguous tensor: a box (box_bytes of the inner
 // dimension x box_rows rows x 1) never crosses from one head into the next, rows past
 // `rows` read as zeros and are not written.  bf16 (d, T, B*H) views, or byte views for
-// e4m3 tensors.
-bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int rows, int inner, bool bytes, int box_rows) {
+// e4m3 tensors.  128-byte boxes use the 128-byte swizzle, narrower ones none.
+bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int rows, int inner, bool bytes, int box_rows,
+                       int box_bytes) {
   const DriverFns& fns = driver_fns();
   if (!fns.encode_tiled) return false;
   const cuuint64_t es = bytes ? 1 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * es, static_cast<cuuint64_t>(rows) * inner * es};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_bytes / es), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   return fns.encode_tiled(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -153,7 +155,7 @@ bool encode_tensor_map(CUtensorMap* map, const void* base, int BH, int rows, int
 // memory, so a cached descriptor is exactly what encoding again would give).
 struct MapCacheEntry {
   const void* base = nullptr;
-  int BH = 0, T = 0, d = 0, box_rows = 0;
+  int BH = 0, T = 0, d = 0, box_rows = 0, box_bytes = 0;
   bool bytes = false;
   CUtensorMap map;
 };
@@ -162,20 +164,22 @@ MapCacheEntry g_map_cache[kMapCache];
 std::mutex g_map_mu;
 
 bool make_tensor_map(CUtensorMap* map, const void* base, int BH, int T, int d, bool bytes = false,
-                     int box_rows = 128) {
+                     int box_rows = 128, int box_bytes = 128) {
   const size_t slot = ((reinterpret_cast<uintptr_t>(base) >> 8) + (box_rows == 128 ? 0 : 1)) % kMapCache;
   std::lock_guard<std::mutex> lock(g_map_mu);
   MapCacheEntry& e = g_map_cache[slot];
-  if (e.base == base && e.BH == BH && e.T == T && e.d == d && e.bytes == bytes && e.box_rows == box_rows) {
+  if (e.base == base && e.BH == BH && e.T == T && e.d == d && e.bytes == bytes && e.box_rows == box_rows &&
+      e.box_bytes == box_bytes) {
     *map = e.map;
     return true;
   }
-  if (!encode_tensor_map(map, base, BH, T, d, bytes, box_rows)) return false;
+  if (!encode_tensor_map(map, base, BH, T, d, bytes, box_rows, box_bytes)) return false;
   e.base = base;
   e.BH = BH;
   e.T = T;
   e.d = d;
   e.box_rows = box_rows;
+  e.box_bytes = box_bytes;
   e.bytes = bytes;
   e.map = *map;
   return true;
@@ -497,9 +501,12 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     for (int b = a + 1; b < 4; ++b)
       if (overlaps(outs[a].p, outs[a].n, outs[b].p, outs[b].n)) return FA_ERR_ALIAS;
   }
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;  // outputs: 32-row x 32-column boxes, no swizzle
   if (!make_tensor_map(&tq, q, BH, T, d) || !make_tensor_map(&tk, k, BH, T, d) ||
-      !make_tensor_map(&tv, v, BH, T, d) || !make_tensor_map(&tdo, dout, BH, T, d))
+      !make_tensor_map(&tv, v, BH, T, d) || !make_tensor_map(&tdo, dout, BH, T, d) ||
+      !make_tensor_map(&tdq, dq, BH, T, d, false, fa::kGradBoxRows, fa::kGradBoxCols * 2) ||
+      !make_tensor_map(&tdk, dk, BH, T, d, false, fa::kGradBoxRows, fa::kGradBoxCols * 2) ||
+      !make_tensor_map(&tdv, dv, BH, T, d, false, fa::kGradBoxRows, fa::kGradBoxCols * 2))
     return FA_ERR_CUDA;
   fa::BwdParams p{};
   p.o = static_cast<const __nv_bfloat16*>(o);
@@ -521,8 +528,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.timeout_ns = kWaitLimitNs;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   if (fa::launch_bwd_rowdot(d, p, num_sms, stream) != cudaSuccess ||
-      fa::launch_bwd_dq(d, tq, tk, tv, tdo, p, grid, stream) != cudaSuccess ||
-      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, p, grid, stream) != cudaSuccess) {
+      fa::launch_bwd_dq(d, tq, tk, tv, tdo, tdq, tdq, p, grid, stream) != cudaSuccess ||
+      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdv, tdk, p, grid, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }

@@ -56,7 +56,10 @@ struct BwdLayout {
   static constexpr int RES_OFF = 0;                  // two resident tiles
   static constexpr int RING_OFF = 2 * TILE;
   static constexpr int VEC_OFF = RING_OFF + STAGES * TILE;  // [2 buffers][LSE*log2e, D][128] fp32
-  static constexpr int BAR_OFF = VEC_OFF + 2 * 2 * BT * 4;
+  // gradient staging: per row warp one 32-row x 32-column bf16 box (2 KB, rows of 64 bytes)
+  static constexpr int STG_OFF = VEC_OFF + 2 * 2 * BT * 4;
+  static constexpr int STG_WARP_BYTES = 32 * 64;
+  static constexpr int BAR_OFF = STG_OFF + ROW_WARPS * STG_WARP_BYTES;
   // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2]
   static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4;  // + s_free, dp_full, dp_free, pv_done
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -120,26 +123,45 @@ __device__ __forceinline__ int bwd_unit_of(int k, int b, int G) { return k * G +
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 
+// Each lane reads 16 bytes (8 elements) of O and of dO; D / 8 lanes cover a row, so a
+// warp pass covers 256 / D rows, and each lane keeps two passes' loads in flight.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
-  constexpr int CPL = D / 32;
+  constexpr int LPR = D / 8;     // lanes per row
+  constexpr int RPW = 32 / LPR;  // rows per warp pass
+  constexpr int U = 2;           // passes per iteration
   const int lane = threadIdx.x % 32;
+  const int sub = lane / LPR, part = lane % LPR;
   const size_t rows = static_cast<size_t>(p.BH) * p.T;
-  const size_t warps = gridDim.x * (blockDim.x / 32);
-  for (size_t r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < rows; r += warps) {
-    const __nv_bfloat16* o = p.o + r * D + lane * CPL;
-    const __nv_bfloat16* g = p.dout + r * D + lane * CPL;
-    float acc = 0.f;
+  const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
+  const size_t w0 = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  for (size_t base = w0 * RPW * U; base < rows; base += warps * RPW * U) {
+    uint4 a[U], b[U];
 #pragma unroll
-    for (int c = 0; c < CPL; c += 2) {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + c));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(g + c));
-      acc = fmaf(a.x, b.x, acc);
-      acc = fmaf(a.y, b.y, acc);
+    for (int u = 0; u < U; ++u) {
+      const size_t r = base + u * RPW + sub;
+      a[u] = b[u] = make_uint4(0, 0, 0, 0);
+      if (r < rows) {
+        a[u] = __ldg(reinterpret_cast<const uint4*>(p.o + r * D) + part);
+        b[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + r * D) + part);
+      }
     }
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) p.drow[r] = acc;
+    for (int u = 0; u < U; ++u) {
+      const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+      const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b[u]);
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float2 xf = __bfloat1622float2(x[c]), yf = __bfloat1622float2(y[c]);
+        acc = fmaf(xf.x, yf.x, acc);
+        acc = fmaf(xf.y, yf.y, acc);
+      }
+#pragma unroll
+      for (int s = LPR / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+      const size_t r = base + u * RPW + sub;
+      if (part == 0 && r < rows) p.drow[r] = acc;
+    }
   }
 }
 
@@ -440,7 +462,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
 // stored as well as dS^T.
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem,
-                                         float* vec) {
+                                         float* vec, uint32_t stg, const CUtensorMap* g1, const CUtensorMap* g2) {
   using SC = BwdSched<D, KIND>;
   constexpr int HC = BT / 2;  // columns per half
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -456,6 +478,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
   uint32_t sf = 0, dpf = 0, pvd = 0, of = 0;
   int it = 0;  // steps so far (vector buffer, first pv_done wait)
   bool ok = true;
+  bool stg_busy = false;  // a TMA store from this warp's staging box may still be reading it
   for (int k = 0; ok && k * G < p.num_units; ++k) {
     const int w = bwd_unit_of(k, blockIdx.x, G);
     if (w >= p.num_units) continue;
@@ -465,15 +488,22 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     const size_t ri = static_cast<size_t>(bh) * p.T + row;
     const float lse2_row = (KIND == 0 && row < p.T) ? p.lse[ri] * LOG2E : 0.f;
     const float d_row = (KIND == 0 && row < p.T) ? p.drow[ri] : 0.f;
+    // KIND 1: the value this thread puts in the step's vector (half 0: LSE * log2 e of query
+    // c0 + r, half 1: its D), loaded one step ahead so the load's latency is off the step
+    auto vec_value = [&](int tt) -> float {
+      const int q = (first + tt) * BT + r;
+      const size_t qi = static_cast<size_t>(bh) * p.T + q;
+      return h == 0 ? (q < p.T ? p.lse[qi] * LOG2E : INFINITY)  // queries past T: P = 0
+                    : (q < p.T ? p.drow[qi] : 0.f);
+    };
+    float vnext = (KIND == 1) ? vec_value(0) : 0.f;
     for (int t = 0; t < n; ++t, ++it) {
       const int c0 = (first + t) * BT;  // first column of the step: a key (KIND 0) or query (KIND 1)
       const float* lv = vec + (it & 1) * 2 * BT + HC * h;  // KIND 1: this half's LSE * log2 e; + BT: D
       if (KIND == 1) {  // half 0 writes the tile's LSE * log2 e, half 1 its D
-        const int q = c0 + r;
-        const size_t qi = static_cast<size_t>(bh) * p.T + q;
         float* lw = vec + (it & 1) * 2 * BT + h * BT;
-        lw[r] = h == 0 ? (q < p.T ? p.lse[qi] * LOG2E : INFINITY)  // queries past T: P = 0
-                       : (q < p.T ? p.drow[qi] : 0.f);
+        lw[r] = vnext;
+        if (t + 1 < n) vnext = vec_value(t + 1);
         mbar_arrive(B.vec_full + 8 * (it & 1));
         if (!(ok = W.wait(B.vec_full + 8 * (it & 1), (it >> 1) & 1))) break;
       }
@@ -579,9 +609,12 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     if (!(ok = W.wait(B.o_full, of))) break;
     of ^= 1;
     tc_fence_after();
+    // the warp's 32 rows x 32 columns at a time through its staging box, one TMA store each
+    // (rows past T lie outside the output map and are not written)
+    const int y0 = r0 + q4 * 32;
 #pragma unroll
     for (int part = 0; part < (KIND == 0 ? 1 : 2); ++part) {  // KIND 0: dQ; KIND 1: dV, then dK
-      __nv_bfloat16* out = (KIND == 0 ? p.dq : (part ? p.dk : p.dv)) + ri * D;
+      const CUtensorMap* gm = part ? g2 : g1;
       const float f = (KIND == 0 || part) ? p.scale : 1.f;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {  // this half's columns of the accumulator
@@ -591,10 +624,20 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * f, u2f(v[2 * e + 1]) * f);
-        if (row < p.T) {
-          uint4* dst = reinterpret_cast<uint4*>(out + col);
+        if (stg_busy) {  // the previous box must have been read out of the staging box
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+        }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        for (int e = 0; e < 4; ++e) st_shared_v4(stg + lane * 64 + e * 16, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (y0 < p.T) {
+          if (lane == 0) {
+            tma_store_3d(gm, stg, col, y0, bh);
+            bulk_commit_group();
+          }
+          stg_busy = true;
         }
       }
     }
@@ -602,12 +645,15 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     __syncwarp();
     if (lane == 0) mbar_arrive(B.o_empty);
   }
+  if (stg_busy && lane == 0) bulk_wait_group0();  // this warp's gradient stores have completed
+  __syncwarp();
 }
 
 template <int D, int KIND>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+              const __grid_constant__ CUtensorMap tmG1, const __grid_constant__ CUtensorMap tmG2, const BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -626,6 +672,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
   }
+  if (warp == 0 && threadIdx.x % 32 == 0) {
+    tma_prefetch_desc(&tmG1);
+    if (KIND == 1) tma_prefetch_desc(&tmG2);
+  }
   pdl_launch_dependents();
   pdl_wait();
   if (warp == BWD_PRODUCER) {
@@ -638,14 +688,16 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     bwd_mma<D, KIND>(p, W, B, sbase, tmem);
     __syncwarp();
   } else {
-    bwd_rows<D, KIND>(p, W, B, tmem, reinterpret_cast<float*>(smem + L::VEC_OFF));
+    bwd_rows<D, KIND>(p, W, B, tmem, reinterpret_cast<float*>(smem + L::VEC_OFF),
+                      sbase + L::STG_OFF + warp * L::STG_WARP_BYTES, &tmG1, &tmG2);
   }
   bwd_teardown<D>(tmem, warp);
 }
 
 template <int D, int KIND>
 cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
-                       const BwdParams& p, int grid, cudaStream_t stream) {
+                       const CUtensorMap& g1, const CUtensorMap& g2, const BwdParams& p, int grid,
+                       cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -666,14 +718,15 @@ cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_bwd_kernel<D, KIND>, q, k, v, dout, p);
+  return cudaLaunchKernelEx(&cfg, fa_bwd_kernel<D, KIND>, q, k, v, dout, g1, g2, p);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.BH) * p.T;
-  const size_t blocks = (rows + 7) / 8;
+  const size_t per_block = static_cast<size_t>(8) * (256 / d) * 2;  // warps x rows per pass x passes
+  const size_t blocks = (rows + per_block - 1) / per_block;
   const int grid = static_cast<int>(blocks < static_cast<size_t>(num_sms) * 8 ? blocks : num_sms * 8);
   if (d == 64)
     fa_bwd_rowdot_kernel<64><<<grid, 256, 0, stream>>>(p);
@@ -683,13 +736,17 @@ cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream
 }
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream) {
-  return d == 64 ? launch_bwd<64, 0>(q, k, v, dout, p, grid, stream) : launch_bwd<128, 0>(q, k, v, dout, p, grid, stream);
+                          const CUtensorMap& dout, const CUtensorMap& g1, const CUtensorMap& g2, const BwdParams& p,
+                          int grid, cudaStream_t stream) {
+  return d == 64 ? launch_bwd<64, 0>(q, k, v, dout, g1, g2, p, grid, stream)
+                 : launch_bwd<128, 0>(q, k, v, dout, g1, g2, p, grid, stream);
 }
 
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream) {
-  return d == 64 ? launch_bwd<64, 1>(q, k, v, dout, p, grid, stream) : launch_bwd<128, 1>(q, k, v, dout, p, grid, stream);
+                            const CUtensorMap& dout, const CUtensorMap& g1, const CUtensorMap& g2,
+                            const BwdParams& p, int grid, cudaStream_t stream) {
+  return d == 64 ? launch_bwd<64, 1>(q, k, v, dout, g1, g2, p, grid, stream)
+                 : launch_bwd<128, 1>(q, k, v, dout, g1, g2, p, grid, stream);
 }
 
 int fa_bwd_smem_bytes(int d) { return d == 64 ? BwdLayout<64>::SMEM : BwdLayout<128>::SMEM; }

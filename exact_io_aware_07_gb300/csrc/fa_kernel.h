@@ -83,11 +83,18 @@ struct BwdParams {
 // D_t = sum_c dO_tc O_tc for every row (one warp per row).
 cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream);
 // dQ: one CTA per SM, units (head, 128-row query tile), key tiles streamed.
+// Gradient outputs (dQ, dK, dV: bf16 (d, T, B*H), no swizzle) are written in boxes of
+// kGradBoxRows rows x kGradBoxCols columns: a row warp's 32 rows and 32 of its columns.
+constexpr int kGradBoxRows = 32;
+constexpr int kGradBoxCols = 32;
+// g1, g2: the output maps (dQ kernel: dQ, and g2 unused; dK/dV kernel: dV, dK).
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream);
+                          const CUtensorMap& dout, const CUtensorMap& g1, const CUtensorMap& g2, const BwdParams& p,
+                          int grid, cudaStream_t stream);
 // dK, dV: one CTA per SM, units (head, 128-key tile), query tiles streamed.
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const BwdParams& p, int grid, cudaStream_t stream);
+                            const CUtensorMap& dout, const CUtensorMap& g1, const CUtensorMap& g2,
+                            const BwdParams& p, int grid, cudaStream_t stream);
 int fa_bwd_smem_bytes(int d);
 // Reads and clears the backward kernels' device status word (bit 0: a wait ran out).
 cudaError_t read_and_clear_bwd_status(cudaStream_t stream, unsigned int* out);
