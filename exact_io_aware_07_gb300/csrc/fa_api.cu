@@ -467,7 +467,8 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
 
 size_t fa_bwd_workspace_bytes(int B, int H, int T) {
   if (B < 1 || H < 1 || T < 1) return 0;
-  const size_t bytes = static_cast<size_t>(B) * H * T * 4;
+  const size_t Tp = (static_cast<size_t>(T) + 127) / 128 * 128;
+  const size_t bytes = 2 * static_cast<size_t>(B) * H * Tp * 4;  // D and LSE * log2 e, rows padded to 128
   return (bytes + 255) / 256 * 256;
 }
 
@@ -513,6 +514,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.lse = lse;
   p.drow = static_cast<float*>(workspace);
+  p.Tp = (T + 127) / 128 * 128;
+  p.lse2 = p.drow + static_cast<size_t>(BH) * p.Tp;
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);

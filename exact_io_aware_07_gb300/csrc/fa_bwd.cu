@@ -60,8 +60,9 @@ struct BwdLayout {
   static constexpr int STG_OFF = VEC_OFF + 2 * 2 * BT * 4;
   static constexpr int STG_WARP_BYTES = 32 * 64;
   static constexpr int BAR_OFF = STG_OFF + ROW_WARPS * STG_WARP_BYTES;
-  // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2]
-  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4;  // + s_free, dp_full, dp_free, pv_done
+  // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2],
+  // s_free, dp_full, dp_free, pv_done, vec_empty[2]
+  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
 };
@@ -94,6 +95,7 @@ struct Bars {
   uint32_t res_full, res_empty, ring_full, ring_empty, s_full, p_full, o_full, o_empty, done;
   uint32_t vec_full;  // [2]: the per-step LSE / D vectors of the dK/dV kernel are in shared memory
   uint32_t s_free, dp_full, dp_free, pv_done;  // SPLIT schedule
+  uint32_t vec_empty;  // [2]: every row warp is done with that vector buffer
 };
 
 template <int D>
@@ -115,6 +117,7 @@ __device__ __forceinline__ Bars make_bars(uint32_t base) {
   b.dp_full = x + 64;
   b.dp_free = x + 72;
   b.pv_done = x + 80;
+  b.vec_empty = x + 88;
   return b;
 }
 
@@ -123,8 +126,9 @@ __device__ __forceinline__ int bwd_unit_of(int k, int b, int G) { return k * G +
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 
-// Each lane reads 16 bytes (8 elements) of O and of dO; D / 8 lanes cover a row, so a
-// warp pass covers 256 / D rows, and each lane keeps two passes' loads in flight.
+// Over the workspace's padded rows (Tp per head): D_t and LSE_t * log2 e for t < T, 0 and
+// +inf past T.  Each lane reads 16 bytes (8 elements) of O and of dO; D / 8 lanes cover a
+// row, so a warp pass covers 256 / D rows, and each lane keeps two passes' loads in flight.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
   constexpr int LPR = D / 8;     // lanes per row
@@ -132,18 +136,22 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
   constexpr int U = 2;           // passes per iteration
   const int lane = threadIdx.x % 32;
   const int sub = lane / LPR, part = lane % LPR;
-  const size_t rows = static_cast<size_t>(p.BH) * p.T;
+  const size_t rows = static_cast<size_t>(p.BH) * p.Tp;
   const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
   const size_t w0 = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   for (size_t base = w0 * RPW * U; base < rows; base += warps * RPW * U) {
     uint4 a[U], b[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const size_t r = base + u * RPW + sub;
+      const size_t r = base + u * RPW + sub;  // padded row: head r / Tp, position r % Tp
       a[u] = b[u] = make_uint4(0, 0, 0, 0);
       if (r < rows) {
-        a[u] = __ldg(reinterpret_cast<const uint4*>(p.o + r * D) + part);
-        b[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + r * D) + part);
+        const size_t bh = r / p.Tp, t = r - bh * p.Tp;
+        if (t < static_cast<size_t>(p.T)) {
+          const size_t src = bh * p.T + t;
+          a[u] = __ldg(reinterpret_cast<const uint4*>(p.o + src * D) + part);
+          b[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + src * D) + part);
+        }
       }
     }
 #pragma unroll
@@ -160,7 +168,12 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
 #pragma unroll
       for (int s = LPR / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
       const size_t r = base + u * RPW + sub;
-      if (part == 0 && r < rows) p.drow[r] = acc;
+      if (part == 0 && r < rows) {
+        const size_t bh = r / p.Tp, t = r - bh * p.Tp;
+        const bool in = t < static_cast<size_t>(p.T);
+        p.drow[r] = acc;  // 0 past T (both rows were read as zeros)
+        p.lse2[r] = in ? p.lse[bh * p.T + t] * LOG2E : INFINITY;
+      }
     }
   }
 }
@@ -184,8 +197,10 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint
     mbar_init(B.o_full, 1);
     mbar_init(B.o_empty, ROW_WARPS);
     mbar_init(B.done, 1);
-    mbar_init(B.vec_full, 32 * ROW_WARPS);
-    mbar_init(B.vec_full + 8, 32 * ROW_WARPS);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(B.vec_full + 8 * b, 1);
+      mbar_init(B.vec_empty + 8 * b, ROW_WARPS);
+    }
     mbar_init(B.s_free, ROW_WARPS);
     mbar_init(B.dp_full, 1);
     mbar_init(B.dp_free, ROW_WARPS);
@@ -246,6 +261,8 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
   uint32_t phase = 0, issued = 0, issued_parity = 0;
   bool res_issued = false, ok = true;
   uint32_t res_parity = 0;
+  int vi = 0;  // dK/dV kernel: steps whose LSE / D vectors have been requested
+  uint32_t vec_issued = 0, vec_parity = 0;
   for (int k = 0; ok && k * G < p.num_units; ++k) {
     const int w = bwd_unit_of(k, blockIdx.x, G);
     if (w >= p.num_units) continue;
@@ -262,6 +279,18 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
     res_parity = nu & 1;
     ++nu;
     for (int t = 0; ok && t < 2 * n; ++t) {
+      if (KIND == 1 && !(t & 1)) {  // the step's LSE * log2 e and D vectors (512 bytes each)
+        const int vb = vi & 1;
+        if (!(ok = wait_all(W, B.vec_empty + 8 * vb, ((vi >> 1) & 1) ^ 1))) break;
+        const uint32_t dst = sbase + L::VEC_OFF + vb * 2 * BT * 4;
+        const size_t off = static_cast<size_t>(bh) * p.Tp + static_cast<size_t>(first + (t >> 1)) * BT;
+        mbar_arrive_expect_tx_elect(B.vec_full + 8 * vb, 2 * BT * 4);
+        bulk_load_elect(dst, p.lse2 + off, BT * 4, B.vec_full + 8 * vb);
+        bulk_load_elect(dst + BT * 4, p.drow + off, BT * 4, B.vec_full + 8 * vb);
+        vec_issued |= 1u << vb;
+        vec_parity = (vec_parity & ~(1u << vb)) | (uint32_t((vi >> 1) & 1) << vb);
+        ++vi;
+      }
       if (!(ok = wait_all(W, B.ring_empty + 8 * stage, phase ^ 1))) break;
       mbar_arrive_expect_tx_elect(B.ring_full + 8 * stage, L::TILE);
 #pragma unroll
@@ -280,6 +309,8 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
     if (res_issued) drain_all(W, B.res_full, res_parity);
     for (int s = 0; s < L::STAGES; ++s)
       if (issued & (1u << s)) drain_all(W, B.ring_full + 8 * s, (issued_parity >> s) & 1u);
+    for (int b = 0; b < 2; ++b)
+      if (vec_issued & (1u << b)) drain_all(W, B.vec_full + 8 * b, (vec_parity >> b) & 1u);
   }
 }
 
@@ -485,26 +516,13 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     int bh, rt, first, n;
     bwd_decode<KIND>(p, w, bh, rt, first, n);
     const int r0 = rt * BT, row = r0 + r;  // this thread's query (KIND 0) or key (KIND 1)
-    const size_t ri = static_cast<size_t>(bh) * p.T + row;
-    const float lse2_row = (KIND == 0 && row < p.T) ? p.lse[ri] * LOG2E : 0.f;
-    const float d_row = (KIND == 0 && row < p.T) ? p.drow[ri] : 0.f;
-    // KIND 1: the value this thread puts in the step's vector (half 0: LSE * log2 e of query
-    // c0 + r, half 1: its D), loaded one step ahead so the load's latency is off the step
-    auto vec_value = [&](int tt) -> float {
-      const int q = (first + tt) * BT + r;
-      const size_t qi = static_cast<size_t>(bh) * p.T + q;
-      return h == 0 ? (q < p.T ? p.lse[qi] * LOG2E : INFINITY)  // queries past T: P = 0
-                    : (q < p.T ? p.drow[qi] : 0.f);
-    };
-    float vnext = (KIND == 1) ? vec_value(0) : 0.f;
+    const size_t rp = static_cast<size_t>(bh) * p.Tp + row;  // the row in the padded workspace
+    const float lse2_row = KIND == 0 ? p.lse2[rp] : 0.f;      // +inf past T: P = 0 there
+    const float d_row = KIND == 0 ? p.drow[rp] : 0.f;
     for (int t = 0; t < n; ++t, ++it) {
       const int c0 = (first + t) * BT;  // first column of the step: a key (KIND 0) or query (KIND 1)
       const float* lv = vec + (it & 1) * 2 * BT + HC * h;  // KIND 1: this half's LSE * log2 e; + BT: D
-      if (KIND == 1) {  // half 0 writes the tile's LSE * log2 e, half 1 its D
-        float* lw = vec + (it & 1) * 2 * BT + h * BT;
-        lw[r] = vnext;
-        if (t + 1 < n) vnext = vec_value(t + 1);
-        mbar_arrive(B.vec_full + 8 * (it & 1));
+      if (KIND == 1) {  // the producer has copied the step's LSE * log2 e and D vectors
         if (!(ok = W.wait(B.vec_full + 8 * (it & 1), (it >> 1) & 1))) break;
       }
       // columns valid for this row: KIND 0 keys < min(T, row + 1) (causal); KIND 1 queries >= row
@@ -525,22 +543,30 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
       uint32_t pp[HC / 2];  // P as bf16 pairs
 #pragma unroll
       for (int c = 0; c < HC / 32; ++c) {
+        float4 l4[8];  // KIND 1: the chunk's LSE * log2 e, read before the Tensor Memory load
+        if (KIND == 1) {
+#pragma unroll
+          for (int f = 0; f < 8; ++f) l4[f] = *reinterpret_cast<const float4*>(lv + 32 * c + 4 * f);
+        }
         uint32_t sv[32];
         tmem_ld32_wait(t_s + 32 * c, sv);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int cc = 32 * c + 2 * e;
           float l0 = lse2_row, l1 = lse2_row;
           if (KIND == 1) {
-            const float2 l2 = *reinterpret_cast<const float2*>(lv + cc);
-            l0 = l2.x;
-            l1 = l2.y;
+            l0 = (e & 1) ? l4[e / 2].z : l4[e / 2].x;
+            l1 = (e & 1) ? l4[e / 2].w : l4[e / 2].y;
           }
-          float p0 = ex2_approx(fmaf(u2f(sv[2 * e]), sl2, -l0));
-          float p1 = ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, -l1));
-          if (cc >= lim || cc < lo) p0 = 0.f;
-          if (cc + 1 >= lim || cc + 1 < lo) p1 = 0.f;
+          const float p0 = ex2_approx(fmaf(u2f(sv[2 * e]), sl2, -l0));
+          const float p1 = ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, -l1));
           pp[16 * c + e] = pack_bf16x2(p0, p1);
+        }
+      }
+      if (lim < HC || lo > 0) {  // a diagonal or ragged tile: masked entries of P become +0
+#pragma unroll
+        for (int e = 0; e < HC / 2; ++e) {
+          if (2 * e >= lim || 2 * e < lo) pp[e] &= 0xFFFF0000u;
+          if (2 * e + 1 >= lim || 2 * e + 1 < lo) pp[e] &= 0x0000FFFFu;
         }
       }
       if (SC::SPLIT) {  // S may now be overwritten by the next step's; P waits for the previous products
@@ -567,23 +593,30 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
       uint32_t pdk[KIND == 0 ? HC / 2 : 1];
 #pragma unroll
       for (int c = 0; c < HC / 32; ++c) {
+        float4 d4[8];  // KIND 1: the chunk's D, read before the Tensor Memory load
+        if (KIND == 1) {
+#pragma unroll
+          for (int f = 0; f < 8; ++f) d4[f] = *reinterpret_cast<const float4*>(lv + BT + 32 * c + 4 * f);
+        }
         uint32_t dv[32];
         tmem_ld32_wait(t_dp + 32 * c, dv);
         uint32_t pd[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int cc = 32 * c + 2 * e;
           float d0 = d_row, d1 = d_row;
           if (KIND == 1) {
-            const float2 dd = *reinterpret_cast<const float2*>(lv + BT + cc);
-            d0 = dd.x;
-            d1 = dd.y;
+            d0 = (e & 1) ? d4[e / 2].z : d4[e / 2].x;
+            d1 = (e & 1) ? d4[e / 2].w : d4[e / 2].y;
           }
           const uint32_t pw = pp[16 * c + e];
           pd[e] = pack_bf16x2(u2f(pw << 16) * (u2f(dv[2 * e]) - d0), u2f(pw & 0xFFFF0000u) * (u2f(dv[2 * e + 1]) - d1));
           if (KIND == 0) pdk[16 * c + e] = pd[e];
         }
         if (KIND == 1) tmem_st16(t_ds + 16 * c, pd);
+      }
+      if (KIND == 1) {  // this warp is done with the step's vectors
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.vec_empty + 8 * (it & 1));
       }
       if (SC::SPLIT) {  // dP may now be overwritten by the next step's
         if (KIND == 1) tmem_wait_st();
@@ -724,7 +757,7 @@ cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 }  // namespace
 
 cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream) {
-  const size_t rows = static_cast<size_t>(p.BH) * p.T;
+  const size_t rows = static_cast<size_t>(p.BH) * p.Tp;
   const size_t per_block = static_cast<size_t>(8) * (256 / d) * 2;  // warps x rows per pass x passes
   const size_t blocks = (rows + per_block - 1) / per_block;
   const int grid = static_cast<int>(blocks < static_cast<size_t>(num_sms) * 8 ? blocks : num_sms * 8);

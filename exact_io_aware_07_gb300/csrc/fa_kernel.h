@@ -67,12 +67,16 @@ struct BwdParams {
   const __nv_bfloat16* o;     // (B*H, T, d) forward output
   const __nv_bfloat16* dout;  // (B*H, T, d) upstream gradient
   const float* lse;           // (B*H, T) forward log-sum-exp (natural log)
-  float* drow;                // (B*H, T) workspace: D_t = sum_c dO_tc O_tc
+  // workspace, rows padded to Tp per head: D_t = sum_c dO_tc O_tc (0 past T) and
+  // LSE_t * log2 e (+inf past T, so that P = 0 there)
+  float* drow;                // (B*H, Tp)
+  float* lse2;                // (B*H, Tp)
   __nv_bfloat16* dq;          // (B*H, T, d) outputs
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int BH, T, causal;
   int nt;                     // 128-row tiles per head: ceil(T / 128)
+  int Tp;                     // nt * 128
   int num_units;              // BH * nt
   float scale;                // softmax scale
   float scale_log2;           // scale * log2(e) (e4m3: times the Q and K scales)
@@ -80,7 +84,7 @@ struct BwdParams {
   unsigned long long timeout_ns;
 };
 
-// D_t = sum_c dO_tc O_tc for every row (one warp per row).
+// D_t = sum_c dO_tc O_tc and LSE_t * log2 e for every row of the padded workspace.
 cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream);
 // dQ: one CTA per SM, units (head, 128-row query tile), key tiles streamed.
 // Gradient outputs (dQ, dK, dV: bf16 (d, T, B*H), no swizzle) are written in boxes of

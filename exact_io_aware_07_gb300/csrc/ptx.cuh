@@ -343,6 +343,14 @@ __device__ __forceinline__ void tma_load_3d_elect(uint32_t dst, const void* tmap
       " [%0], [%1, {%2, %3, %4}], [%5];\n\t}"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
 }
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to shared memory, completing `bytes` on `bar`.
+__device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_l2_3d_elect(const void* tmap, int x, int y, int z) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"

@@ -191,8 +191,8 @@ size_t fa_fwd_fp8_workspace_bytes(int B, int H, int T, int d);
  *   lse              : (B, H, T) fp32, natural log.
  *   dq, dk, dv       : (B, H, T, d) bf16 outputs, overwritten.
  *   workspace        : device memory of at least fa_bwd_workspace_bytes(B, H, T)
- *                      bytes, 16-byte aligned (it receives D; nothing in it needs
- *                      to be set beforehand).
+ *                      bytes, 16-byte aligned (it receives D and LSE * log2 e per
+ *                      row; nothing in it needs to be set beforehand).
  * Three kernels run in order on `stream`: D, then dQ (one unit per 128-row query
  * tile), then dK and dV (one unit per 128-key tile); no output is accumulated
  * across units, so the result does not depend on scheduling.
@@ -206,7 +206,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int B, int H, int T, int d, int causal, float scale,
                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace fa_bwd needs: B * H * T * 4 bytes rounded up to 256; 0 for sizes out of range. */
+/* Workspace fa_bwd needs: 2 * B * H * Tp * 4 bytes (Tp = T rounded up to 128), rounded up
+ * to 256; 0 for sizes out of range. */
 size_t fa_bwd_workspace_bytes(int B, int H, int T);
 
 /* Size of the fixed device scratch fa_fwd_splitkv_noalloc uses (32 MiB). */

@@ -116,3 +116,11 @@ def test_splitkv_checks_inputs_first(lib):
     # the shared checks run before the workspace is looked at
     rc = lib.fa_fwd_splitkv(0, A, A, A, A, 1, 2, 128, 64, 0, ctypes.c_float(0.125), 2, A, 1 << 20, None)
     assert rc == 1
+
+
+def test_bwd_workspace_size(lib):
+    # D and LSE * log2 e for every row, each head's rows padded to a multiple of 128
+    assert fa.fa_bwd_workspace_bytes(1, 4, 1000) == (2 * 4 * 1024 * 4 + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_bytes(2, 3, 128) == 2 * 6 * 128 * 4
+    for bad in ((0, 1, 1), (1, 0, 1), (1, 1, 0)):
+        assert fa.fa_bwd_workspace_bytes(*bad) == 0
