@@ -297,6 +297,13 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
       for (int b = 0; b < L::BOXES; ++b)
         tma_load_3d_elect(sbase + L::RING_OFF + stage * L::TILE + b * BOX, (t & 1) ? mapD : mapC, b * 64,
                           (first + (t >> 1)) * BT, bh, B.ring_full + 8 * stage);
+      // the same tensor's tile two steps on into L2: the ring can hold only two steps, and a
+      // stage is free only once the step that holds it has finished
+      if ((t >> 1) + 2 < n) {
+#pragma unroll
+        for (int b = 0; b < L::BOXES; ++b)
+          tma_prefetch_l2_3d_elect((t & 1) ? mapD : mapC, b * 64, (first + (t >> 1) + 2) * BT, bh);
+      }
       issued |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == L::STAGES) {
