@@ -266,6 +266,10 @@ def run_ours(args, world, rank, local, pg):
         "achieved_isolated_launch": round(f_step / launch_iso_s / 1e12, 2),
         "launch_us_isolated": round(launch_iso_s * 1e6, 2),
     }
+    # the exponential unit's ceiling: one ex2 per unmasked score against 4 d tensor FLOPs
+    ex2_rate = fa.fa_ex2_rate(stream)
+    roofline["ex2_per_s"] = float(f"{ex2_rate:.4g}")
+    roofline["sfu_limited_tflops"] = round(ex2_rate * 4 * d / 1e12, 1)
 
     e2e = run_e2e(fa, torch, dev, w, qkv, scale, min(K, args.e2e_steps), pg) if not args.no_e2e else None
     if e2e is not None:

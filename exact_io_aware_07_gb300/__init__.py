@@ -8,14 +8,17 @@ the library has not been built, importing works but the first call raises.
 
 Entry points (same names as the C ABI):
     fa_fwd(q, k, v, o, lse, causal, scale, stream=None)
+    fa_fwd_gqa(q, k, v, o, lse, causal, scale, stream=None)
+    fa_fwd_paged(q, k_pages, v_pages, block_table, o, lse, causal, scale, stream=None)
+    fa_fwd_fp8(q8, k8, v8, o, lse, causal, scale, descales, workspace, stream=None)
     fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, workspace, stream=None)
     fa_fwd_splitkv_noalloc(q, k, v, o, lse, causal, scale, num_splits, stream=None)
-    fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale, workspace, stream=None)
+    fa_fwd_splitkv_workspace_bytes, fa_fwd_fp8_workspace_bytes, fa_bwd_workspace_bytes
     fa_status_string(code), fa_device_status(stream=None), fa_selftest_wait_timeout(us, stream=None)
-    fa_fwd_launch_shape(B, H, T, d, causal, num_sms), fa_version()
-and the convenience wrappers ``attention(q, k, v, causal, scale=None)`` and
-``attention_splitkv(q, k, v, causal, num_splits, scale=None)`` that allocate O,
-LSE (and the split workspace) with PyTorch.
+    fa_fwd_launch_shape(B, H, T, d, causal, num_sms), fa_ex2_rate(stream=None), fa_version()
+and the convenience wrappers ``attention``, ``attention_gqa``, ``attention_splitkv``
+and ``attention_bwd`` that allocate their outputs (and workspaces) with PyTorch.
 """
 from __future__ import annotations
 
@@ -28,7 +31,7 @@ from ._build import build, lib_path  # noqa: F401
 __all__ = [
     "FAError", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
     "fa_status_string", "fa_device_status", "FA_NOALLOC_SCRATCH_BYTES",
-    "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version",
+    "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_ex2_rate", "fa_version",
     "attention", "attention_splitkv", "load_library", "STATUS", "FA_MAX_SPLITS",
 ]
 
@@ -41,7 +44,8 @@ STATUS = {
 FA_MAX_SPLITS = 256
 EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_fwd_paged", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_bwd",
             "fa_bwd_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
-            "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_version"]
+            "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_ex2_rate",
+            "fa_version"]
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -95,6 +99,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
     lib.fa_selftest_wait_timeout.restype = i
+    lib.fa_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
+    lib.fa_ex2_rate.restype = i
     lib.fa_version.argtypes = []
     lib.fa_version.restype = ctypes.c_char_p
     if path == lib_path():
@@ -144,6 +150,15 @@ def fa_selftest_wait_timeout(timeout_us: int, stream=None) -> None:
     code = load_library().fa_selftest_wait_timeout(int(timeout_us), ctypes.c_void_p(_stream_handle(stream)))
     if code:
         raise FAError(code, "fa_selftest_wait_timeout")
+
+
+def fa_ex2_rate(stream=None) -> float:
+    """ex2.approx operations per second of the current device (a short probe; synchronous)."""
+    out = ctypes.c_double(0.0)
+    code = load_library().fa_ex2_rate(ctypes.byref(out), ctypes.c_void_p(_stream_handle(stream)))
+    if code:
+        raise FAError(code, "fa_ex2_rate")
+    return float(out.value)
 
 
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:

@@ -601,6 +601,18 @@ fa_status fa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream)
   return FA_OK;
 }
 
+fa_status fa_ex2_rate(double* ops_per_second, cudaStream_t stream) {
+  if (!ops_per_second) return FA_ERR_NULL_PTR;
+  int dev = 0, num_sms = 0;
+  fa_status st = current_device(&dev, &num_sms);
+  if (st != FA_OK) return st;
+  if (fa::measure_ex2_rate(num_sms, ops_per_second, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
 const char* fa_version(void) { return "0.1.0"; }
 
 }  // extern "C"

@@ -850,6 +850,45 @@ __global__ void fa_wait_selftest_kernel(unsigned long long timeout_ns) {
   if (threadIdx.x == 0) W.wait(smem_u32(&bar), 0);
 }
 
+// Throughput probe of the exponential unit: every thread runs eight independent chains of
+// x <- 2^(-x) (one ex2.approx and one FMA each), so the unit, not latency, sets the rate.
+__device__ float g_ex2_sink;
+__global__ void __launch_bounds__(256) fa_ex2_rate_kernel(int iters) {
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = 0.125f * i + 1e-3f * (threadIdx.x % 32);
+  for (int it = 0; it < iters; ++it)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = ex2_approx(fmaf(x[i], -1.f, 0.f));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s += x[i];
+  if (s == 12345.f) g_ex2_sink = s;  // never true (x stays in [0.5, 1]); keeps the chains live
+}
+
+cudaError_t measure_ex2_rate(int num_sms, double* ops_per_second, cudaStream_t stream) {
+  constexpr int kIters = 4096, kThreads = 256;
+  const int grid = num_sms * 4;
+  cudaEvent_t a = nullptr, b = nullptr;
+  cudaError_t e = cudaEventCreate(&a);
+  if (e == cudaSuccess) e = cudaEventCreate(&b);
+  if (e == cudaSuccess) {
+    fa_ex2_rate_kernel<<<grid, kThreads, 0, stream>>>(kIters);  // warm-up
+    cudaEventRecord(a, stream);
+    fa_ex2_rate_kernel<<<grid, kThreads, 0, stream>>>(kIters);
+    cudaEventRecord(b, stream);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaEventSynchronize(b);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, a, b);
+  if (e == cudaSuccess)
+    *ops_per_second = static_cast<double>(grid) * kThreads * 8.0 * kIters / (static_cast<double>(ms) * 1e-3);
+  if (a) cudaEventDestroy(a);
+  if (b) cudaEventDestroy(b);
+  return e;
+}
+
 // ---------------------------------------------------------------- host side
 
 template <int D, bool PARTIAL, bool F8 = false>

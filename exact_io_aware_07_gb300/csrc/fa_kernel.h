@@ -54,6 +54,9 @@ int fa_fwd_threads(int d);
 int fa_fwd_rows_per_unit();
 cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* out);
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t stream);
+// ex2.approx operations per second of the whole device (two launches of a probe kernel;
+// waits for the second).
+cudaError_t measure_ex2_rate(int num_sms, double* ops_per_second, cudaStream_t stream);
 
 // Size of the fixed device scratch behind fa_fwd_splitkv_noalloc (32 MiB).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;

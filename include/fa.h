@@ -276,6 +276,18 @@ fa_status fa_fwd_launch_shape(int B, int H, int T, int d, int causal, int num_sm
  */
 fa_status fa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
 
+/*
+ * Throughput of the exponential unit the softmax uses (ex2.approx.ftz.f32),
+ * measured on the current device: the whole-device rate in operations per
+ * second, for the SFU-limited attention rate (one exponential per unmasked
+ * score against 4 d tensor FLOPs; "Flash Attention, tiled", the GPU cost
+ * model of exp vs matmul).  Enqueues two short probe launches on `stream` and
+ * waits for them (the call is synchronous).  FA_ERR_NULL_PTR for a NULL
+ * `ops_per_second`, FA_ERR_NO_DEVICE_SUPPORT off sm_103, FA_ERR_LAUNCH if a
+ * launch or the timing fails.
+ */
+fa_status fa_ex2_rate(double* ops_per_second, cudaStream_t stream);
+
 /* Library version, e.g. "0.1.0". */
 const char* fa_version(void);
 

@@ -161,3 +161,12 @@ def test_rejects_bad_pointers():
     assert call(q.data_ptr(), o.data_ptr(), o.data_ptr()) == 11                # LSE aliases O
     torch.cuda.synchronize()
     assert fa.fa_device_status() == 0
+
+
+def test_ex2_rate_probe():
+    import exact_io_aware_07_gb300 as fa
+
+    rate = fa.fa_ex2_rate()
+    # one GB300: 152 SMs at 1-2.1 GHz issuing at most one ex2 per lane per cycle
+    assert 1e12 < rate < 152 * 128 * 2.2e9
+    assert fa.fa_device_status() == 0
