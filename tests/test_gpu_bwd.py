@@ -80,6 +80,41 @@ def test_backward_matches_oracle(B, H, T, d, causal):
     _compare(x, do_bits, grads, o, causal, scale, f"T{T} d{d} causal{causal}")
 
 
+@pytest.mark.parametrize("B,H,T,d,causal", [(20, 16, 256, 64, 1), (10, 16, 384, 128, 0)])
+def test_backward_many_units_per_cta(B, H, T, d, causal):
+    # 640 / 480 units for 152 persistent CTAs: every CTA runs several units, so the
+    # per-step vector buffers and barrier phases carry over from one unit to the next
+    x, do_bits = _inputs(B, H, T, d, seed=53)
+    scale = default_scale(d)
+    _, grads, o = _run(x, do_bits, causal, scale)
+    _compare(x, do_bits, grads, o, causal, scale, f"B{B} H{H} T{T} d{d} causal{causal}")
+
+
+def test_backward_outputs_exactly_covered():
+    """Every element of dQ, dK and dV is written, and nothing past them."""
+    import torch
+
+    import exact_io_aware_07_gb300 as fa
+
+    B, H, T, d = 2, 3, 333, 128
+    x, do_bits = _inputs(B, H, T, d, seed=54)
+    q, k, v = (to_device(None, b) for b in (x.q_bits, x.k_bits, x.v_bits))
+    do = to_device(None, do_bits)
+    o, lse = fa.attention(q, k, v, causal=True, scale=default_scale(d))
+    n = B * H * T * d
+    bufs = [torch.full((n + 4096,), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    for b in bufs:
+        b[n:] = 7.0
+    dq, dk, dv = (b[:n].view(B, H, T, d) for b in bufs)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, T), dtype=torch.uint8, device="cuda")
+    fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, True, default_scale(d), ws)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for b in bufs:
+        assert not torch.isnan(b[:n]).any()
+        assert torch.all(b[n:] == 7.0)
+
+
 def test_backward_deterministic():
     import torch
 
