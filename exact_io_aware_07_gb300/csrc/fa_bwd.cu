@@ -564,9 +564,9 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
             l0 = (e & 1) ? l4[e / 2].z : l4[e / 2].x;
             l1 = (e & 1) ? l4[e / 2].w : l4[e / 2].y;
           }
-          const float p0 = ex2_approx(fmaf(u2f(sv[2 * e]), sl2, -l0));
-          const float p1 = ex2_approx(fmaf(u2f(sv[2 * e + 1]), sl2, -l1));
-          pp[16 * c + e] = pack_bf16x2(p0, p1);
+          float x0, x1;
+          ffma2v(x0, x1, u2f(sv[2 * e]), u2f(sv[2 * e + 1]), sl2, -l0, -l1);
+          pp[16 * c + e] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
         }
       }
       if (lim < HC || lo > 0) {  // a diagonal or ragged tile: masked entries of P become +0
@@ -616,7 +616,9 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
             d1 = (e & 1) ? d4[e / 2].w : d4[e / 2].y;
           }
           const uint32_t pw = pp[16 * c + e];
-          pd[e] = pack_bf16x2(u2f(pw << 16) * (u2f(dv[2 * e]) - d0), u2f(pw & 0xFFFF0000u) * (u2f(dv[2 * e + 1]) - d1));
+          float s0, s1;
+          fmulsub2(s0, s1, u2f(pw << 16), u2f(pw & 0xFFFF0000u), u2f(dv[2 * e]), u2f(dv[2 * e + 1]), d0, d1);
+          pd[e] = pack_bf16x2(s0, s1);
           if (KIND == 0) pdk[16 * c + e] = pd[e];
         }
         if (KIND == 1) tmem_st16(t_ds + 16 * c, pd);

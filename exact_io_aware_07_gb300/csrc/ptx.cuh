@@ -270,6 +270,21 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
       : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
+// (d0, d1) = (a0, a1) * b + (c0, c1), one packed fp32x2 FMA.
+__device__ __forceinline__ void ffma2v(float& d0, float& d1, float a0, float a1, float b, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+// (d0, d1) = (p0, p1) * ((a0, a1) - (b0, b1)): one packed subtract, one packed multiply.
+__device__ __forceinline__ void fmulsub2(float& d0, float& d1, float p0, float p1, float a0, float a1, float b0,
+                                         float b1) {
+  asm("{\n\t.reg .b64 rp, ra, rb, rd;\n\t"
+      "mov.b64 rp, {%2, %3};\n\tmov.b64 ra, {%4, %5};\n\tmov.b64 rb, {%6, %7};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmul.rn.f32x2 rd, rp, rd;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1) : "f"(p0), "f"(p1), "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 // (acc0, acc1) += (a0, a1) on the packed fp32x2 add path.
 __device__ __forceinline__ void fadd2(float& acc0, float& acc1, float a0, float a1) {
   asm("{\n\t.reg .b64 ra, rc;\n\t"
