@@ -48,25 +48,32 @@ constexpr float LOG2E = 1.4426950408889634074f;
 
 __device__ unsigned int g_bwd_status;  // bit 0: a bounded wait ran out
 
-template <int D>
+template <int D, int KIND>
 struct BwdLayout {
   static constexpr int TILE = BT * D * 2;
   static constexpr int BOXES = D / 64;
-  static constexpr int STAGES = (D == 128) ? 4 : 6;  // streamed tiles in flight
+  // The dQ kernel at d = 128 takes a fifth ring stage in place of the gradient staging (its
+  // dQ rows are stored directly): its key tile K_j stays in the ring until dQ += dS K_j, and
+  // with four stages the loads of the next tiles could not keep up.
+  static constexpr bool DIRECT_OUT = (D == 128 && KIND == 0);
+  static constexpr int STAGES = (D == 128) ? (DIRECT_OUT ? 5 : 4) : 6;  // streamed tiles in flight
   static constexpr int RES_OFF = 0;                  // two resident tiles
   static constexpr int RING_OFF = 2 * TILE;
-  static constexpr int VEC_OFF = RING_OFF + STAGES * TILE;  // [2 buffers][LSE*log2e, D][128] fp32
+  static constexpr int VEC_OFF = RING_OFF + STAGES * TILE;  // dK/dV: [2 buffers][LSE*log2e, D][128] fp32
+  static constexpr int VEC_BYTES = KIND == 1 ? 2 * 2 * BT * 4 : 0;
   // gradient staging: per row warp one 32-row x 32-column bf16 box (2 KB, rows of 64 bytes)
-  static constexpr int STG_OFF = VEC_OFF + 2 * 2 * BT * 4;
+  static constexpr int STG_OFF = VEC_OFF + VEC_BYTES;
   static constexpr int STG_WARP_BYTES = 32 * 64;
-  static constexpr int BAR_OFF = STG_OFF + ROW_WARPS * STG_WARP_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + (DIRECT_OUT ? 0 : ROW_WARPS * STG_WARP_BYTES);
   // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2],
   // s_free, dp_full, dp_free, pv_done, vec_empty[2]
   static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
 };
-static_assert(BwdLayout<128>::SMEM <= 232448 && BwdLayout<64>::SMEM <= 232448, "shared memory over the limit");
+static_assert(BwdLayout<128, 0>::SMEM <= 232448 && BwdLayout<128, 1>::SMEM <= 232448 &&
+                  BwdLayout<64, 0>::SMEM <= 232448 && BwdLayout<64, 1>::SMEM <= 232448,
+              "shared memory over the limit");
 
 // Tensor Memory columns (512 allocated):
 //   dQ kernel:         S [0,128)    dP [128,256)    dQ [256,256+d)  dS [384,448)
@@ -98,9 +105,9 @@ struct Bars {
   uint32_t vec_empty;  // [2]: every row warp is done with that vector buffer
 };
 
-template <int D>
+template <int D, int KIND>
 __device__ __forceinline__ Bars make_bars(uint32_t base) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KIND>;
   Bars b;
   b.res_full = base;
   b.res_empty = base + 8;
@@ -181,10 +188,10 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
 // Common prologue: barriers, Tensor Memory, abort flag.  Returns the TMEM base.
-template <int D>
+template <int D, int KIND>
 __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint32_t* tmem_slot,
                                               volatile int* abort_flag, int warp) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KIND>;
   if (threadIdx.x == 0) {
     mbar_init(B.res_full, 1);
     mbar_init(B.res_empty, 1);
@@ -255,7 +262,7 @@ template <int D, int KIND>
 __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t sbase,
                                              const CUtensorMap* mapA, const CUtensorMap* mapB,
                                              const CUtensorMap* mapC, const CUtensorMap* mapD) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KIND>;
   const int G = gridDim.x;
   int stage = 0, nu = 0;
   uint32_t phase = 0, issued = 0, issued_parity = 0;
@@ -333,7 +340,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t sbase,
                                         uint32_t tmem) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KIND>;
   using SC = BwdSched<D, KIND>;
   constexpr uint32_t IDESC_S = make_idesc_bf16(BT, BT, 0);  // both operands K-major (d contiguous)
   constexpr uint32_t IDESC_G = make_idesc_bf16(BT, D, 1);   // B MN-major: rows of d contiguous elements
@@ -501,6 +508,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem,
                                          float* vec, uint32_t stg, const CUtensorMap* g1, const CUtensorMap* g2) {
+  using L = BwdLayout<D, KIND>;
   using SC = BwdSched<D, KIND>;
   constexpr int HC = BT / 2;  // columns per half
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -652,10 +660,28 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     of ^= 1;
     tc_fence_after();
     // the warp's 32 rows x 32 columns at a time through its staging box, one TMA store each
-    // (rows past T lie outside the output map and are not written)
+    // (rows past T lie outside the output map and are not written); without a staging box
+    // (the d = 128 dQ kernel) each thread stores its row directly
     const int y0 = r0 + q4 * 32;
+    if (L::DIRECT_OUT) {
+      __nv_bfloat16* out = p.dq + (static_cast<size_t>(bh) * p.T + row) * D;
 #pragma unroll
-    for (int part = 0; part < (KIND == 0 ? 1 : 2); ++part) {  // KIND 0: dQ; KIND 1: dV, then dK
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = h * (D / 2) + 32 * c;
+        uint32_t v[32];
+        tmem_ld32_wait(t_acc + col, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * p.scale, u2f(v[2 * e + 1]) * p.scale);
+        if (row < p.T) {
+          uint4* dst = reinterpret_cast<uint4*>(out + col);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int part = 0; !L::DIRECT_OUT && part < (KIND == 0 ? 1 : 2); ++part) {  // KIND 0: dQ; KIND 1: dV, then dK
       const CUtensorMap* gm = part ? g2 : g1;
       const float f = (KIND == 0 || part) ? p.scale : 1.f;
 #pragma unroll
@@ -696,15 +722,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmG1, const __grid_constant__ CUtensorMap tmG2, const BwdParams p) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const Bars B = make_bars<D>(sbase + L::BAR_OFF);
+  const Bars B = make_bars<D, KIND>(sbase + L::BAR_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
   const int warp = threadIdx.x / 32;
-  const uint32_t tmem = bwd_setup<D>(smem, B, tmem_slot, abort_flag, warp);
+  const uint32_t tmem = bwd_setup<D, KIND>(smem, B, tmem_slot, abort_flag, warp);
   const Waiter W{abort_flag, p.timeout_ns, &g_bwd_status};
   // the set-up above overlaps the previous kernel's tail; memory is read only after it has
   // finished (the tensor maps are kernel parameters, so fetching them may start earlier)
@@ -746,14 +772,14 @@ cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
     e = cudaFuncSetAttribute(fa_bwd_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             BwdLayout<D>::SMEM);
+                             BwdLayout<D, KIND>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(BWD_THREADS);
-  cfg.dynamicSmemBytes = BwdLayout<D>::SMEM;
+  cfg.dynamicSmemBytes = BwdLayout<D, KIND>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -791,7 +817,9 @@ cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& q, const CUtensorMap& k, c
                  : launch_bwd<128, 1>(q, k, v, dout, g1, g2, p, grid, stream);
 }
 
-int fa_bwd_smem_bytes(int d) { return d == 64 ? BwdLayout<64>::SMEM : BwdLayout<128>::SMEM; }
+int fa_bwd_smem_bytes(int d) {
+  return d == 64 ? max(BwdLayout<64, 0>::SMEM, BwdLayout<64, 1>::SMEM) : max(BwdLayout<128, 0>::SMEM, BwdLayout<128, 1>::SMEM);
+}
 
 cudaError_t read_and_clear_bwd_status(cudaStream_t stream, unsigned int* out) {
   cudaError_t e = cudaStreamSynchronize(stream);
