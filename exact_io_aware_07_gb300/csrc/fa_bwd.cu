@@ -52,13 +52,16 @@ template <int D, int KIND>
 struct BwdLayout {
   static constexpr int TILE = BT * D * 2;
   static constexpr int BOXES = D / 64;
-  // The dQ kernel at d = 128 takes a fifth ring stage in place of the gradient staging (its
-  // dQ rows are stored directly): its key tile K_j stays in the ring until dQ += dS K_j, and
+  // The dQ kernel at d = 128 keeps dO in Tensor Memory (the A operand of dP = dO V^T, in the
+  // 64 columns its schedule leaves free) and stores dQ rows directly, so that its shared
+  // memory holds six ring stages: its key tile K_j stays in the ring until dQ += dS K_j, and
   // with four stages the loads of the next tiles could not keep up.
-  static constexpr bool DIRECT_OUT = (D == 128 && KIND == 0);
-  static constexpr int STAGES = (D == 128) ? (DIRECT_OUT ? 5 : 4) : 6;  // streamed tiles in flight
-  static constexpr int RES_OFF = 0;                  // two resident tiles
-  static constexpr int RING_OFF = 2 * TILE;
+  static constexpr bool DO_TMEM = (D == 128 && KIND == 0);
+  static constexpr bool DIRECT_OUT = DO_TMEM;
+  static constexpr int STAGES = (D == 128) ? (DO_TMEM ? 6 : 4) : 6;  // streamed tiles in flight
+  static constexpr int RES_TILES = DO_TMEM ? 1 : 2;  // resident tiles in shared memory
+  static constexpr int RES_OFF = 0;
+  static constexpr int RING_OFF = RES_TILES * TILE;
   static constexpr int VEC_OFF = RING_OFF + STAGES * TILE;  // dK/dV: [2 buffers][LSE*log2e, D][128] fp32
   static constexpr int VEC_BYTES = KIND == 1 ? 2 * 2 * BT * 4 : 0;
   // gradient staging: per row warp one 32-row x 32-column bf16 box (2 KB, rows of 64 bytes)
@@ -66,8 +69,8 @@ struct BwdLayout {
   static constexpr int STG_WARP_BYTES = 32 * 64;
   static constexpr int BAR_OFF = STG_OFF + (DIRECT_OUT ? 0 : ROW_WARPS * STG_WARP_BYTES);
   // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2],
-  // s_free, dp_full, dp_free, pv_done, vec_empty[2]
-  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2;
+  // s_free, dp_full, dp_free, pv_done, vec_empty[2], do_full
+  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
 };
@@ -83,6 +86,7 @@ static_assert(BwdLayout<128, 0>::SMEM <= 232448 && BwdLayout<128, 1>::SMEM <= 23
 // With P / dS in columns of their own (SPLIT), the next step's S and dP are issued as soon
 // as the row warps have read this step's, so the products overlap the row-warp work.
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256, COL_BUF = 384;
+constexpr uint32_t COL_DO = 448;  // d = 128 dQ kernel: dO as bf16 pairs (after dS [384, 448))
 template <int D, int KIND>
 struct BwdSched {
   static constexpr bool SPLIT = (KIND == 0) || (D == 64);
@@ -103,6 +107,7 @@ struct Bars {
   uint32_t vec_full;  // [2]: the per-step LSE / D vectors of the dK/dV kernel are in shared memory
   uint32_t s_free, dp_full, dp_free, pv_done;  // SPLIT schedule
   uint32_t vec_empty;  // [2]: every row warp is done with that vector buffer
+  uint32_t do_full;    // the unit's dO is in Tensor Memory (d = 128 dQ kernel)
 };
 
 template <int D, int KIND>
@@ -125,6 +130,7 @@ __device__ __forceinline__ Bars make_bars(uint32_t base) {
   b.dp_free = x + 72;
   b.pv_done = x + 80;
   b.vec_empty = x + 88;
+  b.do_full = x + 104;
   return b;
 }
 
@@ -212,6 +218,7 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint
     mbar_init(B.dp_full, 1);
     mbar_init(B.dp_free, ROW_WARPS);
     mbar_init(B.pv_done, 1);
+    mbar_init(B.do_full, ROW_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -276,11 +283,12 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
     int bh, rt, first, n;
     bwd_decode<KIND>(p, w, bh, rt, first, n);
     if (!(ok = wait_all(W, B.res_empty, (nu & 1) ^ 1))) break;
-    mbar_arrive_expect_tx_elect(B.res_full, 2 * L::TILE);
+    mbar_arrive_expect_tx_elect(B.res_full, L::RES_TILES * L::TILE);
 #pragma unroll
     for (int b = 0; b < L::BOXES; ++b) {
       tma_load_3d_elect(sbase + L::RES_OFF + b * BOX, mapA, b * 64, rt * BT, bh, B.res_full);
-      tma_load_3d_elect(sbase + L::RES_OFF + L::TILE + b * BOX, mapB, b * 64, rt * BT, bh, B.res_full);
+      if (L::RES_TILES == 2)
+        tma_load_3d_elect(sbase + L::RES_OFF + L::TILE + b * BOX, mapB, b * 64, rt * BT, bh, B.res_full);
     }
     res_issued = true;
     res_parity = nu & 1;
@@ -350,7 +358,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
   const uint32_t dm_lo = uint32_t(dm), dm_hi = uint32_t(dm >> 32);
   const int G = gridDim.x;
   int stage = 0, nu = 0;
-  uint32_t phase = 0, pf = 0, oe = 0, sfr = 0, dpf = 0;
+  uint32_t phase = 0, pf = 0, oe = 0, sfr = 0, dpf = 0, dof = 0;
   bool ok = true;
 #define BWD_TAKE(slot)                                                   \
   {                                                                      \
@@ -376,6 +384,19 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
       mma_ss_elect(tmem + (col), dk_lo + ((L::RES_OFF + (r) * L::TILE) >> 4) + off, dk_hi,                  \
                    dk_lo + ((L::RING_OFF + (st) * L::TILE) >> 4) + off, dk_hi, IDESC_S, kk > 0 ? 1u : 0u);   \
     }                                                                                                      \
+  }
+// dP (or dP^T) = [resident tile 1] x [streamed tile in stage st]^T; the d = 128 dQ kernel
+// takes dO from Tensor Memory instead (A operand as bf16 pairs, B the V tile K-major)
+#define BWD_DP(st)                                                                                        \
+  {                                                                                                       \
+    if (L::DO_TMEM) {                                                                                     \
+      _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                             \
+        const uint32_t off = ((kk / 4) * BOX + (kk % 4) * 32) >> 4;                                       \
+        mma_ts_elect(tmem + COL_DP, tmem + COL_DO + kk * 8, dk_lo + ((L::RING_OFF + (st) * L::TILE) >> 4) + off, \
+                     dk_hi, IDESC_S, kk > 0 ? 1u : 0u);                                                   \
+      }                                                                                                   \
+    } else                                                                                                \
+      BWD_SCORE(COL_DP, 1, st);                                                                           \
   }
 // accumulator col += (bf16 pairs at column a) x [streamed tile in stage st] (MN-major)
 #define BWD_GRAD(col, a, st, acc0)                                                                         \
@@ -419,7 +440,8 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
           BWD_WAIT(B.dp_free, par);
           dpf ^= 1;
         }
-        BWD_SCORE(COL_DP, 1, s1);
+        if (L::DO_TMEM) BWD_WAIT(B.do_full, dof);  // the row warps have put the unit's dO in place
+        BWD_DP(s1);
         mma_commit_elect(B.dp_full);
       } while (0);
       if (!ok) break;
@@ -441,7 +463,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
           BWD_WAIT(B.dp_free, par);
           dpf ^= 1;
         }
-        BWD_SCORE(COL_DP, 1, n1);
+        BWD_DP(n1);
         mma_commit_elect(B.dp_full);
       }
       if (t == 0) {
@@ -487,6 +509,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
 #undef BWD_TAKE
 #undef BWD_WAIT
 #undef BWD_SCORE
+#undef BWD_DP
 #undef BWD_GRAD
   // every MMA and commit arrival has landed before Tensor Memory is freed
   mma_commit_elect(B.done);
@@ -534,6 +557,26 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     const size_t rp = static_cast<size_t>(bh) * p.Tp + row;  // the row in the padded workspace
     const float lse2_row = KIND == 0 ? p.lse2[rp] : 0.f;      // +inf past T: P = 0 there
     const float d_row = KIND == 0 ? p.drow[rp] : 0.f;
+    if (L::DO_TMEM) {  // this half of the row's dO, as bf16 pairs, into Tensor Memory (every
+                       // product of the previous unit has finished: its epilogue waited for o_full)
+      const uint4* src = reinterpret_cast<const uint4*>(p.dout + (static_cast<size_t>(bh) * p.T + row) * D + h * 64);
+      uint32_t dw[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 x = row < p.T ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        dw[4 * c] = x.x;
+        dw[4 * c + 1] = x.y;
+        dw[4 * c + 2] = x.z;
+        dw[4 * c + 3] = x.w;
+      }
+      const uint32_t t_do = tmem + lane_off + COL_DO + 32 * h;
+      tmem_st16(t_do, *reinterpret_cast<const uint32_t(*)[16]>(dw));
+      tmem_st16(t_do + 16, *reinterpret_cast<const uint32_t(*)[16]>(dw + 16));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.do_full);
+    }
     for (int t = 0; t < n; ++t, ++it) {
       const int c0 = (first + t) * BT;  // first column of the step: a key (KIND 0) or query (KIND 1)
       const float* lv = vec + (it & 1) * 2 * BT + HC * h;  // KIND 1: this half's LSE * log2 e; + BT: D
