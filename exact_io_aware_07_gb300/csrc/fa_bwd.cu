@@ -7,23 +7,28 @@
 //   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q.
 //
 // Three kernels, no atomics and no T x T matrix in memory:
-//   fa_bwd_rowdot_kernel  D for every row (one warp per row);
-//   fa_bwd_dq_kernel      per (head, 128-row query tile): stream the key tiles,
-//                         S = Q K^T and dP = dO V^T on the tensor core, dS in the
-//                         softmax warps, dQ += dS K (dS read from Tensor Memory);
-//   fa_bwd_dkdv_kernel    per (head, 128-key tile): stream the query tiles,
-//                         S^T = K Q^T and dP^T = V dO^T, P^T and dS^T in the
-//                         softmax warps, dV += P^T dO and dK += dS^T Q (P^T and
-//                         dS^T read from Tensor Memory).
+//   fa_bwd_rowdot_kernel      D and LSE * log2 e for every row, into a workspace whose rows
+//                             are padded per head to a multiple of 128 (D = 0 and
+//                             LSE * log2 e = +inf there, so P = 0 without a mask);
+//   fa_bwd_kernel<d, 0> (dQ)  per (head, 128-row query tile): stream the key tiles,
+//                             S = Q K^T and dP = dO V^T on the tensor core, dS in the
+//                             row warps, dQ += dS K (dS read from Tensor Memory; at
+//                             d = 128 dO is kept in Tensor Memory too);
+//   fa_bwd_kernel<d, 1>       per (head, 128-key tile): stream the query tiles and their
+//     (dK, dV)                LSE / D vectors, S^T = K Q^T and dP^T = V dO^T, P^T and dS^T
+//                             in the row warps, dV += P^T dO and dK += dS^T Q (P^T and
+//                             dS^T read from Tensor Memory).
 // Each recomputes S and dP (seven matrix products per tile pair instead of
-// five) so that every product takes its A operand from Tensor Memory with the
-// rows it needs on the lanes, and no partial sum crosses CTAs.
+// five) so that every gradient product takes its A operand from Tensor Memory
+// with the rows it needs on the lanes, and no partial sum crosses CTAs.  The
+// gradients leave through shared memory and TMA stores (32 x 32 boxes), except
+// dQ at d = 128, whose shared memory holds a sixth ring stage instead.
 //
 // Roles (320 threads, one CTA per SM, persistent over work units):
 //   warps 0-7  row warps: one TMEM lane (one row of the unit's 128-row tile) per
 //              thread, warps w and w + 4 splitting the row's 128 columns
-//   warp 8     TMA producer: the unit's two resident tiles, then the streamed
-//              tiles through a ring
+//   warp 8     TMA producer: the unit's resident tiles, then the streamed tiles
+//              (and the dK/dV kernel's per-step vectors) through a ring
 //   warp 9     Tensor Memory allocator and tcgen05.mma issuer (whole warp,
 //              elect.sync picks the issuing lane)
 // Every mbarrier wait is bounded; on expiry the kernel records it in its
@@ -79,7 +84,7 @@ static_assert(BwdLayout<128, 0>::SMEM <= 232448 && BwdLayout<128, 1>::SMEM <= 23
               "shared memory over the limit");
 
 // Tensor Memory columns (512 allocated):
-//   dQ kernel:         S [0,128)    dP [128,256)    dQ [256,256+d)  dS [384,448)
+//   dQ kernel:         S [0,128)    dP [128,256)    dQ [256,256+d)  dS [384,448)  (d = 128: dO [448,512))
 //   dK/dV kernel d=64: S^T [0,128)  dP^T [128,256)  dV [256,320)  dK [320,384)  P^T [384,448)  dS^T [448,512)
 //   dK/dV kernel d=128: S^T, dP^T as above, dV [256,384), dK [384,512); P^T and dS^T are
 //     written over the first 64 columns of S^T and dP^T.

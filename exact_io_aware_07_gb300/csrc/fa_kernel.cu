@@ -41,6 +41,9 @@
 // P_1 [448,512) have columns of their own, so S_i(j+1) is computed while the
 // softmax of S_i(j) runs, and each tile's MMAs are issued by a warp of its own
 // that waits only on that tile's barriers.
+// O leaves through shared memory: each softmax warp writes its 32 rows x 64
+// columns in the 128-byte swizzled layout of the output tensor map and one lane
+// stores them with a TMA tensor store, so every store moves whole rows.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
