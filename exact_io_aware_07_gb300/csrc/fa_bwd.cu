@@ -86,8 +86,8 @@ static_assert(BwdLayout<128, 0>::SMEM <= 232448 && BwdLayout<128, 1>::SMEM <= 23
 // Tensor Memory columns (512 allocated):
 //   dQ kernel:         S [0,128)    dP [128,256)    dQ [256,256+d)  dS [384,448)  (d = 128: dO [448,512))
 //   dK/dV kernel d=64: S^T [0,128)  dP^T [128,256)  dV [256,320)  dK [320,384)  P^T [384,448)  dS^T [448,512)
-//   dK/dV kernel d=128: S^T, dP^T as above, dV [256,384), dK [384,512); P^T and dS^T are
-//     written over the first 64 columns of S^T and dP^T.
+//   dK/dV kernel d=128: S^T, dP^T as above, dV [256,384), dK [384,512); dS^T and P^T are
+//     written over dP^T (each row warp over the 64 columns of dP^T it has read itself).
 // With P / dS in columns of their own (SPLIT), the next step's S and dP are issued as soon
 // as the row warps have read this step's, so the products overlap the row-warp work.
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256, COL_BUF = 384;
@@ -97,13 +97,14 @@ struct BwdSched {
   static constexpr bool SPLIT = (KIND == 0) || (D == 64);
   // Packed (bf16-pair) column of the 16-wide K step kk of P / dS, relative to COL_P / COL_DS.
   // The row warps of column half h write pairs for columns [64h, 64h + 64): contiguous in their
-  // own buffers (SPLIT), or over the first half of the S / dP columns they read themselves.
+  // own buffers (SPLIT), or over the dP columns they read themselves.
   static __device__ __forceinline__ constexpr uint32_t a_col(int kk) {
     return SPLIT ? uint32_t(kk) * 8u : uint32_t(kk / 4) * 64u + uint32_t(kk % 4) * 8u;
   }
   static __device__ __forceinline__ constexpr uint32_t half_col(int h) { return SPLIT ? 32u * h : 64u * h; }
-  // where the row warps put P (dK/dV kernel) and dS (both kernels)
-  static constexpr uint32_t COL_P = SPLIT ? COL_BUF : COL_S;
+  // where the row warps put P (dK/dV kernel) and dS (both kernels); without SPLIT the row
+  // warps of half h write dS over dP columns [64h, 64h + 32) and P over [64h + 32, 64h + 64)
+  static constexpr uint32_t COL_P = SPLIT ? COL_BUF : COL_DP + 32;
   static constexpr uint32_t COL_DS = SPLIT ? (KIND == 0 ? COL_BUF : COL_BUF + 64) : COL_DP;
 };
 
@@ -348,8 +349,10 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
 //   S(t+1) once the row warps have read S(t) (s_free), dP(t+1) once they have read
 //   dP(t) (dp_free), and the gradient products of step t once P / dS are written
 //   (p_full), committing pv_done, which the row warps wait on before they overwrite
-//   P / dS.  Otherwise P / dS are written over S / dP, and step t+1's products follow
-//   step t's gradient products.
+//   P / dS.  Otherwise (the d = 128 dK/dV kernel, whose accumulators fill half of Tensor
+//   Memory) P^T / dS^T are written over dP^T: S^T(t+1) still goes out once S^T(t) has been
+//   read, but dP^T(t+1) follows step t's gradient products (dK first, so the Q tile's ring
+//   stage is released one product earlier for the load of Q(t+2)).
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t sbase,
                                         uint32_t tmem) {
@@ -420,8 +423,13 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
     tc_fence_after();
     int s0 = 0, s1 = 0;  // ring stages of the current step's two streamed tiles
     if (!SC::SPLIT) {
-      do {  // step 0's two products
+      do {  // step 0's two products (dP^T follows the previous unit's gradient products in issue order)
         BWD_TAKE(s0);
+        {
+          uint32_t par = sfr ^ 1;
+          BWD_WAIT(B.s_free, par);
+          sfr ^= 1;
+        }
         BWD_SCORE(COL_S, 0, s0);
         mma_commit_elect(B.s_full);
         BWD_TAKE(s1);
@@ -470,6 +478,15 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
         }
         BWD_DP(n1);
         mma_commit_elect(B.dp_full);
+      } else if (t + 1 < n) {  // the next S^T, as soon as this step's has been read
+        BWD_TAKE(n0);
+        {
+          uint32_t par = sfr ^ 1;
+          BWD_WAIT(B.s_free, par);
+          sfr ^= 1;
+        }
+        BWD_SCORE(COL_S, 0, n0);
+        mma_commit_elect(B.s_full);
       }
       if (t == 0) {
         uint32_t par = oe ^ 1;
@@ -483,20 +500,15 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
       } else if (SC::SPLIT) {
         BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);       // dV += P^T dO_i
         BWD_GRAD(COL_ACC + D, SC::COL_DS, s0, acc0);  // dK += dS^T Q_i
-      } else {
-        // P^T and dS^T sit over S^T and dP^T: the next step's S^T follows dV (which reads
-        // P^T) and its dP^T follows dK (which reads dS^T), so the row warps can start on the
-        // next S^T while dK and the next dP^T run
-        BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);  // dV += P^T dO_i
-        if (t + 1 < n) {
-          BWD_TAKE(n0);
-          BWD_SCORE(COL_S, 0, n0);
-          mma_commit_elect(B.s_full);
-        }
+      } else {  // P^T and dS^T sit over dP^T
         BWD_GRAD(COL_ACC + D, SC::COL_DS, s0, acc0);  // dK += dS^T Q_i
+        mma_commit_elect(B.ring_empty + 8 * s0);
+        BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);  // dV += P^T dO_i
       }
-      if (SC::SPLIT) mma_commit_elect(B.pv_done);
-      mma_commit_elect(B.ring_empty + 8 * s0);
+      if (SC::SPLIT) {
+        mma_commit_elect(B.pv_done);
+        mma_commit_elect(B.ring_empty + 8 * s0);
+      }
       mma_commit_elect(B.ring_empty + 8 * s1);
       if (!SC::SPLIT && t + 1 < n) {
         BWD_TAKE(n1);
@@ -525,17 +537,18 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
 // the unit's 128-row tile and columns [64h, 64h + 64) with h = w / 4.  Each step:
 //   P = exp(S - LSE) with masked entries 0, packed to bf16 pairs;
 //   dS = P (dP - D), packed to bf16 pairs;
-// and the pairs go to Tensor Memory for the gradient products.  With the SPLIT
-// schedule S and dP are read whole before anything is written (s_free and dp_free
-// let the MMA warp overwrite them with the next step's), and P / dS go to their own
-// columns once the previous step's gradient products are done (pv_done).
+// and the pairs go to Tensor Memory for the gradient products.  S is read whole
+// before anything is written (s_free lets the MMA warp overwrite it with the next
+// step's).  With the SPLIT schedule dP is too (dp_free), and P / dS go to their own
+// columns once the previous step's gradient products are done (pv_done); otherwise
+// they go over the dP columns the warp has read.
 // KIND 0 (dQ): the row is a query; LSE and D are per row, the mask runs along keys.
 // KIND 1 (dK, dV): the row is a key; LSE and D are per column (query), read from the
 // step's vectors in shared memory (every lane reads the same word), and P^T is
 // stored as well as dS^T.
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem,
-                                         float* vec, uint32_t stg, const CUtensorMap* g1, const CUtensorMap* g2) {
+                                         uint32_t vec, uint32_t stg, const CUtensorMap* g1, const CUtensorMap* g2) {
   using L = BwdLayout<D, KIND>;
   using SC = BwdSched<D, KIND>;
   constexpr int HC = BT / 2;  // columns per half
@@ -584,7 +597,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     }
     for (int t = 0; t < n; ++t, ++it) {
       const int c0 = (first + t) * BT;  // first column of the step: a key (KIND 0) or query (KIND 1)
-      const float* lv = vec + (it & 1) * 2 * BT + HC * h;  // KIND 1: this half's LSE * log2 e; + BT: D
+      const uint32_t lv = vec + ((it & 1) * 2 * BT + HC * h) * 4;  // KIND 1: this half's LSE * log2 e; + 4 BT: D
       if (KIND == 1) {  // the producer has copied the step's LSE * log2 e and D vectors
         if (!(ok = W.wait(B.vec_full + 8 * (it & 1), (it >> 1) & 1))) break;
       }
@@ -609,7 +622,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
         float4 l4[8];  // KIND 1: the chunk's LSE * log2 e, read before the Tensor Memory load
         if (KIND == 1) {
 #pragma unroll
-          for (int f = 0; f < 8; ++f) l4[f] = *reinterpret_cast<const float4*>(lv + 32 * c + 4 * f);
+          for (int f = 0; f < 8; ++f) l4[f] = ld_shared_v4f(lv + (32 * c + 4 * f) * 4);
         }
         uint32_t sv[32];
         tmem_ld32_wait(t_s + 32 * c, sv);
@@ -632,17 +645,16 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
           if (2 * e + 1 >= lim || 2 * e + 1 < lo) pp[e] &= 0x0000FFFFu;
         }
       }
-      if (SC::SPLIT) {  // S may now be overwritten by the next step's; P waits for the previous products
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(B.s_free);
-        if (KIND == 1 && it > 0) {
+      // S may now be overwritten by the next step's; with SPLIT, P waits for the previous products
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.s_free);
+      if (SC::SPLIT && KIND == 1) {
+        if (it > 0) {
           if (!(ok = W.wait(B.pv_done, pvd))) break;
           pvd ^= 1;
           tc_fence_after();
         }
-      }
-      if (KIND == 1) {
 #pragma unroll
         for (int c = 0; c < HC / 32; ++c)
           tmem_st16(t_p + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pp + 16 * c));
@@ -650,16 +662,18 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
       if (!(ok = W.wait(B.dp_full, dpf))) break;
       dpf ^= 1;
       tc_fence_after();
-      // dS, 32 columns at a time: stored as it is formed (in place over dP without SPLIT, or into
-      // the dS^T columns once the previous step's products are done), or, in the dQ kernel, kept
-      // until dP is released and the previous dQ product has read the dS columns
+      // dS, 32 columns at a time: stored as it is formed (without SPLIT over the dP columns this
+      // warp has read, chunk c's 16 pairs over the first half of chunk c's 32 columns read so
+      // far; with SPLIT into the dS^T columns once the previous step's products are done), or,
+      // in the dQ kernel, kept until dP is released and the previous dQ product has read the dS
+      // columns
       uint32_t pdk[KIND == 0 ? HC / 2 : 1];
 #pragma unroll
       for (int c = 0; c < HC / 32; ++c) {
         float4 d4[8];  // KIND 1: the chunk's D, read before the Tensor Memory load
         if (KIND == 1) {
 #pragma unroll
-          for (int f = 0; f < 8; ++f) d4[f] = *reinterpret_cast<const float4*>(lv + BT + 32 * c + 4 * f);
+          for (int f = 0; f < 8; ++f) d4[f] = ld_shared_v4f(lv + (BT + 32 * c + 4 * f) * 4);
         }
         uint32_t dv[32];
         tmem_ld32_wait(t_dp + 32 * c, dv);
@@ -678,6 +692,11 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
           if (KIND == 0) pdk[16 * c + e] = pd[e];
         }
         if (KIND == 1) tmem_st16(t_ds + 16 * c, pd);
+      }
+      if (KIND == 1 && !SC::SPLIT) {  // P^T over the second half of this warp's dP^T columns, read above
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c)
+          tmem_st16(t_p + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pp + 16 * c));
       }
       if (KIND == 1) {  // this warp is done with the step's vectors
         __syncwarp();
@@ -804,7 +823,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     bwd_mma<D, KIND>(p, W, B, sbase, tmem);
     __syncwarp();
   } else {
-    bwd_rows<D, KIND>(p, W, B, tmem, reinterpret_cast<float*>(smem + L::VEC_OFF),
+    bwd_rows<D, KIND>(p, W, B, tmem, sbase + L::VEC_OFF,
                       sbase + L::STG_OFF + warp * L::STG_WARP_BYTES, &tmG1, &tmG2);
   }
   bwd_teardown<D>(tmem, warp);
