@@ -524,7 +524,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.causal = causal;
   p.nt = (T + 127) / 128;
   const long long units = static_cast<long long>(BH) * p.nt;
-  if (units > INT_MAX) return FA_ERR_BAD_SHAPE;
+  if (units * 128 > INT_MAX) return FA_ERR_BAD_SHAPE;  // padded rows are indexed in 32 bits
   p.num_units = static_cast<int>(units);
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);

@@ -147,30 +147,33 @@ __device__ __forceinline__ int bwd_unit_of(int k, int b, int G) { return k * G +
 
 // Over the workspace's padded rows (Tp per head): D_t and LSE_t * log2 e for t < T, 0 and
 // +inf past T.  Each lane reads 16 bytes (8 elements) of O and of dO; D / 8 lanes cover a
-// row, so a warp pass covers 256 / D rows, and each lane keeps two passes' loads in flight.
+// row, so a warp pass covers 256 / D rows, and each lane keeps four passes' loads in flight.
+// Row numbers fit 32 bits (the host refuses larger shapes), so the head / position split
+// is one 32-bit division.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
   constexpr int LPR = D / 8;     // lanes per row
   constexpr int RPW = 32 / LPR;  // rows per warp pass
-  constexpr int U = 2;           // passes per iteration
+  constexpr int U = 4;           // passes per iteration
   const int lane = threadIdx.x % 32;
-  const int sub = lane / LPR, part = lane % LPR;
-  const size_t rows = static_cast<size_t>(p.BH) * p.Tp;
-  const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x / 32);
-  const size_t w0 = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
-  for (size_t base = w0 * RPW * U; base < rows; base += warps * RPW * U) {
+  const uint32_t sub = lane / LPR, part = lane % LPR;
+  const uint32_t rows = static_cast<uint32_t>(p.BH) * static_cast<uint32_t>(p.Tp);
+  const uint32_t Tp = static_cast<uint32_t>(p.Tp), T = static_cast<uint32_t>(p.T);
+  const uint32_t warps = gridDim.x * (blockDim.x / 32);
+  const uint32_t w0 = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  for (uint32_t base = w0 * RPW * U; base < rows; base += warps * RPW * U) {
     uint4 a[U], b[U];
+    uint32_t bh[U], t[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const size_t r = base + u * RPW + sub;  // padded row: head r / Tp, position r % Tp
+      const uint32_t r = base + u * RPW + sub;  // padded row: head r / Tp, position r % Tp
+      bh[u] = r / Tp;
+      t[u] = r - bh[u] * Tp;
       a[u] = b[u] = make_uint4(0, 0, 0, 0);
-      if (r < rows) {
-        const size_t bh = r / p.Tp, t = r - bh * p.Tp;
-        if (t < static_cast<size_t>(p.T)) {
-          const size_t src = bh * p.T + t;
-          a[u] = __ldg(reinterpret_cast<const uint4*>(p.o + src * D) + part);
-          b[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + src * D) + part);
-        }
+      if (r < rows && t[u] < T) {
+        const size_t src = static_cast<size_t>(bh[u]) * T + t[u];
+        a[u] = __ldg(reinterpret_cast<const uint4*>(p.o + src * D) + part);
+        b[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + src * D) + part);
       }
     }
 #pragma unroll
@@ -186,12 +189,10 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
       }
 #pragma unroll
       for (int s = LPR / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-      const size_t r = base + u * RPW + sub;
+      const uint32_t r = base + u * RPW + sub;
       if (part == 0 && r < rows) {
-        const size_t bh = r / p.Tp, t = r - bh * p.Tp;
-        const bool in = t < static_cast<size_t>(p.T);
         p.drow[r] = acc;  // 0 past T (both rows were read as zeros)
-        p.lse2[r] = in ? p.lse[bh * p.T + t] * LOG2E : INFINITY;
+        p.lse2[r] = t[u] < T ? p.lse[static_cast<size_t>(bh[u]) * T + t[u]] * LOG2E : INFINITY;
       }
     }
   }
@@ -860,7 +861,7 @@ cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 
 cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.BH) * p.Tp;
-  const size_t per_block = static_cast<size_t>(8) * (256 / d) * 2;  // warps x rows per pass x passes
+  const size_t per_block = static_cast<size_t>(8) * (256 / d) * 4;  // warps x rows per pass x passes
   const size_t blocks = (rows + per_block - 1) / per_block;
   const int grid = static_cast<int>(blocks < static_cast<size_t>(num_sms) * 8 ? blocks : num_sms * 8);
   if (d == 64)

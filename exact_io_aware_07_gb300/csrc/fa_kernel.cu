@@ -236,11 +236,35 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.timeout_ns, &g_status};
   // the set-up above overlaps the previous kernel's tail; inputs are read only after it has
-  // finished (the tensor maps are kernel parameters, so fetching them may start earlier)
+  // finished (the tensor maps are kernel parameters, so fetching them may start earlier).
+  // Before that, the first unit's query tiles and first key / value tiles are pulled into
+  // L2: a prefetch only warms the cache that every write of the previous kernel goes
+  // through, so it cannot return stale data (the block table of paged K/V is input data,
+  // so paged K/V tiles are not prefetched here).
   if (warp == PRODUCER_WARP && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    const int w = unit_of(0, blockIdx.x, G);
+    if (w < p.num_units) {
+      const Unit u = decode_unit<PARTIAL>(p, w);
+      const int nmax = max(u.n0, u.n1);
+      if (nmax > 0) {
+        for (int i = 0; i < 2; ++i)
+          for (int b = 0; b < L::BOXES; ++b) tma_prefetch_l2_3d(&tmQ, b * 64, u.qb * 2 * BM + i * BM, u.bh);
+        if (!p.block_table) {
+          const int kvh = p.group == 1 ? u.bh : (u.bh / p.H) * (p.H / p.group) + (u.bh % p.H) / p.group;
+          for (int j = 0; j < min(nmax, 2); ++j)
+            for (int b = 0; b < L::BOXES; ++b) {
+              tma_prefetch_l2_3d(&tmK, b * 64, (u.jb + j) * BN, kvh);
+              if (F8)
+                tma_prefetch_l2_3d(&tmV, (u.jb + j) * BN, 0, kvh);
+              else
+                tma_prefetch_l2_3d(&tmV, b * 64, (u.jb + j) * BN, kvh);
+            }
+        }
+      }
+    }
   }
   if (!PARTIAL && warp == 0 && lane == 0) tma_prefetch_desc(&tmO);
   pdl_launch_dependents();
