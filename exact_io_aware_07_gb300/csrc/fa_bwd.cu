@@ -801,12 +801,27 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t tmem = bwd_setup<D, KIND>(smem, B, tmem_slot, abort_flag, warp);
   const Waiter W{abort_flag, p.timeout_ns, &g_bwd_status};
   // the set-up above overlaps the previous kernel's tail; memory is read only after it has
-  // finished (the tensor maps are kernel parameters, so fetching them may start earlier)
+  // finished (the tensor maps are kernel parameters, so fetching them may start earlier).
+  // Before that, the first unit's resident tiles and first two streamed tiles are pulled
+  // into L2: a prefetch only warms the cache that every write of the previous kernel goes
+  // through, so it cannot return stale data.
   if (warp == BWD_PRODUCER && threadIdx.x % 32 == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
+    const int w = bwd_unit_of(0, blockIdx.x, gridDim.x);
+    if (w < p.num_units) {
+      int bh, rt, first, n;
+      bwd_decode<KIND>(p, w, bh, rt, first, n);
+      const CUtensorMap* res[2] = {KIND == 0 ? &tmQ : &tmK, KIND == 0 ? &tmDO : &tmV};
+      const CUtensorMap* str[2] = {KIND == 0 ? &tmK : &tmQ, KIND == 0 ? &tmV : &tmDO};
+      for (int b = 0; b < L::BOXES; ++b)
+        for (int m = 0; m < 2; ++m) {
+          tma_prefetch_l2_3d(res[m], b * 64, rt * BT, bh);
+          for (int j = 0; j < min(n, 2); ++j) tma_prefetch_l2_3d(str[m], b * 64, (first + j) * BT, bh);
+        }
+    }
   }
   if (warp == 0 && threadIdx.x % 32 == 0) {
     tma_prefetch_desc(&tmG1);
