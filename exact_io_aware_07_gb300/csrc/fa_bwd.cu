@@ -24,13 +24,17 @@
 // gradients leave through shared memory and TMA stores (32 x 32 boxes), except
 // dQ at d = 128, whose shared memory holds a sixth ring stage instead.
 //
-// Roles (320 threads, one CTA per SM, persistent over work units):
-//   warps 0-7  row warps: one TMEM lane (one row of the unit's 128-row tile) per
-//              thread, warps w and w + 4 splitting the row's 128 columns
-//   warp 8     TMA producer: the unit's resident tiles, then the streamed tiles
-//              (and the dK/dV kernel's per-step vectors) through a ring
-//   warp 9     Tensor Memory allocator and tcgen05.mma issuer (whole warp,
-//              elect.sync picks the issuing lane)
+// Roles (448 threads, one CTA per SM, persistent over work units):
+//   warps 0-7    row warps: one TMEM lane (one row of the unit's 128-row tile) per
+//                thread, warps w and w + 4 splitting the row's 128 columns
+//   warp 8       TMA producer: the unit's resident tiles, then the streamed tiles
+//                (and the dK/dV kernel's per-step vectors) through a ring
+//   warp 9       Tensor Memory allocator and tcgen05.mma issuer (whole warp,
+//                elect.sync picks the issuing lane)
+//   warps 10-13  output warps, one per TMEM lane quarter: the finished unit's
+//                gradients out of Tensor Memory to global memory (and at d = 128 the
+//                dQ kernel's next dO into Tensor Memory) while the row warps start on
+//                the next unit
 // Every mbarrier wait is bounded; on expiry the kernel records it in its
 // status word and unwinds, as the forward kernel does.
 #include <cuda.h>
@@ -44,10 +48,11 @@ namespace fa {
 namespace {
 
 constexpr int BT = 128;  // rows per tile (queries or keys)
-constexpr int BWD_THREADS = 320;
+constexpr int BWD_THREADS = 448;
 constexpr int BWD_PRODUCER = 8;
 constexpr int BWD_MMA = 9;
 constexpr int ROW_WARPS = 8;  // two per TMEM lane quarter, each taking half of the 128 columns
+constexpr int OUT_WARP0 = 10, OUT_WARPS = 4;  // one per TMEM lane quarter
 constexpr int BOX = 128 * 128;  // one TMA box: 128 rows x 64 bf16, 128-byte swizzle
 constexpr float LOG2E = 1.4426950408889634074f;
 
@@ -69,10 +74,10 @@ struct BwdLayout {
   static constexpr int RING_OFF = RES_TILES * TILE;
   static constexpr int VEC_OFF = RING_OFF + STAGES * TILE;  // dK/dV: [2 buffers][LSE*log2e, D][128] fp32
   static constexpr int VEC_BYTES = KIND == 1 ? 2 * 2 * BT * 4 : 0;
-  // gradient staging: per row warp one 32-row x 32-column bf16 box (2 KB, rows of 64 bytes)
+  // gradient staging: per output warp two 32-row x 32-column bf16 boxes (2 KB each, rows of 64 bytes)
   static constexpr int STG_OFF = VEC_OFF + VEC_BYTES;
-  static constexpr int STG_WARP_BYTES = 32 * 64;
-  static constexpr int BAR_OFF = STG_OFF + (DIRECT_OUT ? 0 : ROW_WARPS * STG_WARP_BYTES);
+  static constexpr int STG_BOX_BYTES = 32 * 64;
+  static constexpr int BAR_OFF = STG_OFF + (DIRECT_OUT ? 0 : OUT_WARPS * 2 * STG_BOX_BYTES);
   // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2],
   // s_free, dp_full, dp_free, pv_done, vec_empty[2], do_full
   static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2 + 1;
@@ -215,7 +220,7 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint
     mbar_init(B.s_full, 1);
     mbar_init(B.p_full, ROW_WARPS);
     mbar_init(B.o_full, 1);
-    mbar_init(B.o_empty, ROW_WARPS);
+    mbar_init(B.o_empty, OUT_WARPS);
     mbar_init(B.done, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(B.vec_full + 8 * b, 1);
@@ -225,7 +230,7 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint
     mbar_init(B.dp_full, 1);
     mbar_init(B.dp_free, ROW_WARPS);
     mbar_init(B.pv_done, 1);
-    mbar_init(B.do_full, ROW_WARPS);
+    mbar_init(B.do_full, OUT_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -549,7 +554,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
 // stored as well as dS^T.
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem,
-                                         uint32_t vec, uint32_t stg, const CUtensorMap* g1, const CUtensorMap* g2) {
+                                         uint32_t vec) {
   using L = BwdLayout<D, KIND>;
   using SC = BwdSched<D, KIND>;
   constexpr int HC = BT / 2;  // columns per half
@@ -558,15 +563,13 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
   const int r = q4 * 32 + lane;
   const uint32_t lane_off = uint32_t(q4 * 32) << 16;
   const uint32_t t_s = tmem + lane_off + COL_S + HC * h, t_dp = tmem + lane_off + COL_DP + HC * h;
-  const uint32_t t_acc = tmem + lane_off + COL_ACC;
   const uint32_t t_p = tmem + lane_off + SC::COL_P + SC::half_col(h);
   const uint32_t t_ds = tmem + lane_off + SC::COL_DS + SC::half_col(h);
   const float sl2 = p.scale_log2;
   const int G = gridDim.x;
-  uint32_t sf = 0, dpf = 0, pvd = 0, of = 0;
+  uint32_t sf = 0, dpf = 0, pvd = 0;
   int it = 0;  // steps so far (vector buffer, first pv_done wait)
   bool ok = true;
-  bool stg_busy = false;  // a TMA store from this warp's staging box may still be reading it
   for (int k = 0; ok && k * G < p.num_units; ++k) {
     const int w = bwd_unit_of(k, blockIdx.x, G);
     if (w >= p.num_units) continue;
@@ -576,26 +579,6 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     const size_t rp = static_cast<size_t>(bh) * p.Tp + row;  // the row in the padded workspace
     const float lse2_row = KIND == 0 ? p.lse2[rp] : 0.f;      // +inf past T: P = 0 there
     const float d_row = KIND == 0 ? p.drow[rp] : 0.f;
-    if (L::DO_TMEM) {  // this half of the row's dO, as bf16 pairs, into Tensor Memory (every
-                       // product of the previous unit has finished: its epilogue waited for o_full)
-      const uint4* src = reinterpret_cast<const uint4*>(p.dout + (static_cast<size_t>(bh) * p.T + row) * D + h * 64);
-      uint32_t dw[32];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 x = row < p.T ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        dw[4 * c] = x.x;
-        dw[4 * c + 1] = x.y;
-        dw[4 * c + 2] = x.z;
-        dw[4 * c + 3] = x.w;
-      }
-      const uint32_t t_do = tmem + lane_off + COL_DO + 32 * h;
-      tmem_st16(t_do, *reinterpret_cast<const uint32_t(*)[16]>(dw));
-      tmem_st16(t_do + 16, *reinterpret_cast<const uint32_t(*)[16]>(dw + 16));
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B.do_full);
-    }
     for (int t = 0; t < n; ++t, ++it) {
       const int c0 = (first + t) * BT;  // first column of the step: a key (KIND 0) or query (KIND 1)
       const uint32_t lv = vec + ((it & 1) * 2 * BT + HC * h) * 4;  // KIND 1: this half's LSE * log2 e; + 4 BT: D
@@ -724,25 +707,92 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
       if (lane == 0) mbar_arrive(B.p_full);
     }
     if (!ok) break;
+  }
+}
+
+// This lane's row of dO (d = 128, bf16) into Tensor Memory columns [t_do, t_do + 64) as
+// bf16 pairs: the A operand of the dQ kernel's dP = dO V^T.  Rows past T are zeros.
+__device__ __forceinline__ void bwd_load_do(const BwdParams& p, int bh, int row, uint32_t t_do) {
+  const uint4* src = reinterpret_cast<const uint4*>(p.dout + (static_cast<size_t>(bh) * p.T + row) * 128);
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2) {  // 64 elements (32 pairs) at a time
+    uint32_t dw[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 x = row < p.T ? __ldg(src + 8 * c2 + c) : make_uint4(0, 0, 0, 0);
+      dw[4 * c] = x.x;
+      dw[4 * c + 1] = x.y;
+      dw[4 * c + 2] = x.z;
+      dw[4 * c + 3] = x.w;
+    }
+    tmem_st32(t_do + 32 * c2, dw);
+  }
+  tmem_wait_st();
+}
+
+// Output warps: four, warp w holding rows 32 (w % 4) + lane of the unit's tile and all of
+// the accumulator's columns.  Once a unit's last gradient product is done (o_full) the d = 128
+// dQ kernel first puts the next unit's dO into Tensor Memory (do_full; the first unit's at
+// the start); then the accumulator is read 32 columns at a time, scaled, packed to bf16 and
+// stored -- 32 x 32 boxes through two staging boxes per warp and TMA stores (rows past T lie
+// outside the output map and are not written), or at d = 128 in the dQ kernel, whose shared
+// memory holds no staging, by each thread for its own row -- and o_empty releases the
+// accumulator to the next unit.  The row warps meanwhile start on the next unit.
+template <int D, int KIND>
+__device__ __forceinline__ void bwd_out(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t tmem,
+                                        uint32_t stg, const CUtensorMap* g1, const CUtensorMap* g2) {
+  using L = BwdLayout<D, KIND>;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int q4 = warp % 4;
+  const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+  const uint32_t t_acc = tmem + lane_off + COL_ACC;
+  const int G = gridDim.x;
+  // the first unit index >= k this CTA works on, or -1
+  auto next_unit = [&](int k) -> int {
+    for (; k * G < p.num_units; ++k)
+      if (bwd_unit_of(k, blockIdx.x, G) < p.num_units) return k;
+    return -1;
+  };
+  auto put_do = [&](int k) {  // unit k's dO for this warp's rows, then do_full
+    int bh, rt, first, n;
+    bwd_decode<KIND>(p, bwd_unit_of(k, blockIdx.x, G), bh, rt, first, n);
+    bwd_load_do(p, bh, rt * BT + q4 * 32 + lane, tmem + lane_off + COL_DO);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.do_full);
+  };
+  uint32_t of = 0;
+  bool ok = true;
+  int nb = 0;             // boxes staged so far: the next goes to staging box nb & 1
+  bool stg_busy = false;  // a TMA store may still be reading a staging box
+  if (L::DO_TMEM) {
+    const int k0 = next_unit(0);
+    if (k0 >= 0) put_do(k0);
+  }
+  for (int k = 0; ok && k * G < p.num_units; ++k) {
+    const int w = bwd_unit_of(k, blockIdx.x, G);
+    if (w >= p.num_units) continue;
+    int bh, rt, first, n;
+    bwd_decode<KIND>(p, w, bh, rt, first, n);
     if (!(ok = W.wait(B.o_full, of))) break;
     of ^= 1;
     tc_fence_after();
-    // the warp's 32 rows x 32 columns at a time through its staging box, one TMA store each
-    // (rows past T lie outside the output map and are not written); without a staging box
-    // (the d = 128 dQ kernel) each thread stores its row directly
-    const int y0 = r0 + q4 * 32;
+    if (L::DO_TMEM) {  // every product of this unit has finished reading the dO columns
+      const int k2 = next_unit(k + 1);
+      if (k2 >= 0) put_do(k2);
+    }
+    const int y0 = rt * BT + q4 * 32, row = y0 + lane;
     if (L::DIRECT_OUT) {
       __nv_bfloat16* out = p.dq + (static_cast<size_t>(bh) * p.T + row) * D;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = h * (D / 2) + 32 * c;
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32_wait(t_acc + col, v);
+        tmem_ld32_wait(t_acc + 32 * c, v);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * p.scale, u2f(v[2 * e + 1]) * p.scale);
         if (row < p.T) {
-          uint4* dst = reinterpret_cast<uint4*>(out + col);
+          uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
@@ -753,28 +803,29 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
       const CUtensorMap* gm = part ? g2 : g1;
       const float f = (KIND == 0 || part) ? p.scale : 1.f;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {  // this half's columns of the accumulator
-        const int col = h * (D / 2) + 32 * c;
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32_wait(t_acc + part * D + col, v);
+        tmem_ld32_wait(t_acc + part * D + 32 * c, v);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * f, u2f(v[2 * e + 1]) * f);
-        if (stg_busy) {  // the previous box must have been read out of the staging box
-          if (lane == 0) bulk_wait_group_read0();
+        const uint32_t box = stg + (nb & 1) * L::STG_BOX_BYTES;
+        if (stg_busy) {  // the store two boxes back, which used this staging box, has read it
+          if (lane == 0) bulk_wait_group_read1();
           __syncwarp();
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) st_shared_v4(stg + lane * 64 + e * 16, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        for (int e = 0; e < 4; ++e) st_shared_v4(box + lane * 64 + e * 16, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (y0 < p.T) {
           if (lane == 0) {
-            tma_store_3d(gm, stg, col, y0, bh);
+            tma_store_3d(gm, box, 32 * c, y0, bh);
             bulk_commit_group();
           }
           stg_busy = true;
         }
+        ++nb;
       }
     }
     tc_fence_before();
@@ -823,7 +874,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
     }
   }
-  if (warp == 0 && threadIdx.x % 32 == 0) {
+  if (warp == OUT_WARP0 && threadIdx.x % 32 == 0) {
     tma_prefetch_desc(&tmG1);
     if (KIND == 1) tma_prefetch_desc(&tmG2);
   }
@@ -838,9 +889,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   } else if (warp == BWD_MMA) {
     bwd_mma<D, KIND>(p, W, B, sbase, tmem);
     __syncwarp();
+  } else if (warp >= OUT_WARP0) {
+    bwd_out<D, KIND>(p, W, B, tmem, sbase + L::STG_OFF + (warp - OUT_WARP0) * 2 * L::STG_BOX_BYTES, &tmG1, &tmG2);
   } else {
-    bwd_rows<D, KIND>(p, W, B, tmem, sbase + L::VEC_OFF,
-                      sbase + L::STG_OFF + warp * L::STG_WARP_BYTES, &tmG1, &tmG2);
+    bwd_rows<D, KIND>(p, W, B, tmem, sbase + L::VEC_OFF);
   }
   bwd_teardown<D>(tmem, warp);
 }

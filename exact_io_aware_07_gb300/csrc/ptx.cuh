@@ -73,6 +73,8 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until this thread's bulk groups have finished reading their shared-memory sources.
 __device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until at most one of this thread's bulk groups may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Waits until this thread's bulk groups have completed.
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Orders this thread's ordinary shared-memory writes before later reads of them by the
