@@ -79,8 +79,8 @@ struct BwdLayout {
   static constexpr int STG_BOX_BYTES = 32 * 64;
   static constexpr int BAR_OFF = STG_OFF + (DIRECT_OUT ? 0 : OUT_WARPS * 2 * STG_BOX_BYTES);
   // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2],
-  // s_free, dp_full, dp_free, pv_done, vec_empty[2], do_full
-  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2 + 1;
+  // s_free, dp_full, dp_free, pv_done, vec_empty[2], do_full, p_half
+  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2 + 1 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
 };
@@ -91,8 +91,8 @@ static_assert(BwdLayout<128, 0>::SMEM <= 232448 && BwdLayout<128, 1>::SMEM <= 23
 // Tensor Memory columns (512 allocated):
 //   dQ kernel:         S [0,128)    dP [128,256)    dQ [256,256+d)  dS [384,448)  (d = 128: dO [448,512))
 //   dK/dV kernel d=64: S^T [0,128)  dP^T [128,256)  dV [256,320)  dK [320,384)  P^T [384,448)  dS^T [448,512)
-//   dK/dV kernel d=128: S^T, dP^T as above, dV [256,384), dK [384,512); dS^T and P^T are
-//     written over dP^T (each row warp over the 64 columns of dP^T it has read itself).
+//   dK/dV kernel d=128: S^T, dP^T as above, dV [256,384), dK [384,512); P^T is written over
+//     S^T and dS^T over dP^T (each row warp over the first 32 of the 64 columns it has read).
 // With P / dS in columns of their own (SPLIT), the next step's S and dP are issued as soon
 // as the row warps have read this step's, so the products overlap the row-warp work.
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256, COL_BUF = 384;
@@ -102,14 +102,14 @@ struct BwdSched {
   static constexpr bool SPLIT = (KIND == 0) || (D == 64);
   // Packed (bf16-pair) column of the 16-wide K step kk of P / dS, relative to COL_P / COL_DS.
   // The row warps of column half h write pairs for columns [64h, 64h + 64): contiguous in their
-  // own buffers (SPLIT), or over the dP columns they read themselves.
+  // own buffers (SPLIT), or over the S / dP columns they read themselves.
   static __device__ __forceinline__ constexpr uint32_t a_col(int kk) {
     return SPLIT ? uint32_t(kk) * 8u : uint32_t(kk / 4) * 64u + uint32_t(kk % 4) * 8u;
   }
   static __device__ __forceinline__ constexpr uint32_t half_col(int h) { return SPLIT ? 32u * h : 64u * h; }
   // where the row warps put P (dK/dV kernel) and dS (both kernels); without SPLIT the row
-  // warps of half h write dS over dP columns [64h, 64h + 32) and P over [64h + 32, 64h + 64)
-  static constexpr uint32_t COL_P = SPLIT ? COL_BUF : COL_DP + 32;
+  // warps of half h write P over S columns [64h, 64h + 32) and dS over dP columns [64h, 64h + 32)
+  static constexpr uint32_t COL_P = SPLIT ? COL_BUF : COL_S;
   static constexpr uint32_t COL_DS = SPLIT ? (KIND == 0 ? COL_BUF : COL_BUF + 64) : COL_DP;
 };
 
@@ -119,6 +119,7 @@ struct Bars {
   uint32_t s_free, dp_full, dp_free, pv_done;  // SPLIT schedule
   uint32_t vec_empty;  // [2]: every row warp is done with that vector buffer
   uint32_t do_full;    // the unit's dO is in Tensor Memory (d = 128 dQ kernel)
+  uint32_t p_half;     // P^T is written (d = 128 dK/dV kernel)
 };
 
 template <int D, int KIND>
@@ -142,6 +143,7 @@ __device__ __forceinline__ Bars make_bars(uint32_t base) {
   b.pv_done = x + 80;
   b.vec_empty = x + 88;
   b.do_full = x + 104;
+  b.p_half = x + 112;
   return b;
 }
 
@@ -231,6 +233,7 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint
     mbar_init(B.dp_free, ROW_WARPS);
     mbar_init(B.pv_done, 1);
     mbar_init(B.do_full, OUT_WARPS);
+    mbar_init(B.p_half, ROW_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -356,9 +359,11 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, const Waiter& W
 //   dP(t) (dp_free), and the gradient products of step t once P / dS are written
 //   (p_full), committing pv_done, which the row warps wait on before they overwrite
 //   P / dS.  Otherwise (the d = 128 dK/dV kernel, whose accumulators fill half of Tensor
-//   Memory) P^T / dS^T are written over dP^T: S^T(t+1) still goes out once S^T(t) has been
-//   read, but dP^T(t+1) follows step t's gradient products (dK first, so the Q tile's ring
-//   stage is released one product earlier for the load of Q(t+2)).
+//   Memory) P^T is written over S^T and dS^T over dP^T, and the row warps signal P^T on its
+//   own (p_half): per step the warp issues dV(t) once P^T(t) is written, S^T(t+1) behind it
+//   (it overwrites P^T), dK(t) once dS^T(t) is written, and dP^T(t+1) behind that, so dV and
+//   the next S^T run while the row warps form dS, and dK and the next dP^T while they form
+//   the next P.
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, const Bars& B, uint32_t sbase,
                                         uint32_t tmem) {
@@ -372,7 +377,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
   const uint32_t dm_lo = uint32_t(dm), dm_hi = uint32_t(dm >> 32);
   const int G = gridDim.x;
   int stage = 0, nu = 0;
-  uint32_t phase = 0, pf = 0, oe = 0, sfr = 0, dpf = 0, dof = 0;
+  uint32_t phase = 0, pf = 0, oe = 0, sfr = 0, dpf = 0, dof = 0, phf = 0;
   bool ok = true;
 #define BWD_TAKE(slot)                                                   \
   {                                                                      \
@@ -429,13 +434,8 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
     tc_fence_after();
     int s0 = 0, s1 = 0;  // ring stages of the current step's two streamed tiles
     if (!SC::SPLIT) {
-      do {  // step 0's two products (dP^T follows the previous unit's gradient products in issue order)
+      do {  // step 0's two products (they follow the previous unit's gradient products in issue order)
         BWD_TAKE(s0);
-        {
-          uint32_t par = sfr ^ 1;
-          BWD_WAIT(B.s_free, par);
-          sfr ^= 1;
-        }
         BWD_SCORE(COL_S, 0, s0);
         mma_commit_elect(B.s_full);
         BWD_TAKE(s1);
@@ -484,38 +484,37 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
         }
         BWD_DP(n1);
         mma_commit_elect(B.dp_full);
-      } else if (t + 1 < n) {  // the next S^T, as soon as this step's has been read
-        BWD_TAKE(n0);
-        {
-          uint32_t par = sfr ^ 1;
-          BWD_WAIT(B.s_free, par);
-          sfr ^= 1;
-        }
-        BWD_SCORE(COL_S, 0, n0);
-        mma_commit_elect(B.s_full);
       }
       if (t == 0) {
         uint32_t par = oe ^ 1;
         BWD_WAIT(B.o_empty, par);
         oe ^= 1;
       }
-      BWD_WAIT(B.p_full, pf);
       const uint32_t acc0 = t > 0 ? 1u : 0u;
+      if (!SC::SPLIT) {  // dV(t) once P^T(t) is written, then the next S^T over it
+        BWD_WAIT(B.p_half, phf);
+        BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);  // dV += P^T dO_i
+        mma_commit_elect(B.ring_empty + 8 * s1);
+        if (t + 1 < n) {
+          BWD_TAKE(n0);
+          BWD_SCORE(COL_S, 0, n0);
+          mma_commit_elect(B.s_full);
+        }
+      }
+      BWD_WAIT(B.p_full, pf);
       if (KIND == 0) {
         BWD_GRAD(COL_ACC, SC::COL_DS, s0, acc0);  // dQ += dS K_j
       } else if (SC::SPLIT) {
         BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);       // dV += P^T dO_i
         BWD_GRAD(COL_ACC + D, SC::COL_DS, s0, acc0);  // dK += dS^T Q_i
-      } else {  // P^T and dS^T sit over dP^T
+      } else {  // dS^T sits over dP^T
         BWD_GRAD(COL_ACC + D, SC::COL_DS, s0, acc0);  // dK += dS^T Q_i
-        mma_commit_elect(B.ring_empty + 8 * s0);
-        BWD_GRAD(COL_ACC, SC::COL_P, s1, acc0);  // dV += P^T dO_i
       }
       if (SC::SPLIT) {
         mma_commit_elect(B.pv_done);
-        mma_commit_elect(B.ring_empty + 8 * s0);
+        mma_commit_elect(B.ring_empty + 8 * s1);
       }
-      mma_commit_elect(B.ring_empty + 8 * s1);
+      mma_commit_elect(B.ring_empty + 8 * s0);
       if (!SC::SPLIT && t + 1 < n) {
         BWD_TAKE(n1);
         BWD_SCORE(COL_DP, 1, n1);
@@ -543,11 +542,12 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const Waiter& W, con
 // the unit's 128-row tile and columns [64h, 64h + 64) with h = w / 4.  Each step:
 //   P = exp(S - LSE) with masked entries 0, packed to bf16 pairs;
 //   dS = P (dP - D), packed to bf16 pairs;
-// and the pairs go to Tensor Memory for the gradient products.  S is read whole
-// before anything is written (s_free lets the MMA warp overwrite it with the next
-// step's).  With the SPLIT schedule dP is too (dp_free), and P / dS go to their own
-// columns once the previous step's gradient products are done (pv_done); otherwise
-// they go over the dP columns the warp has read.
+// and the pairs go to Tensor Memory for the gradient products.  With the SPLIT
+// schedule S and dP are read whole before anything is written (s_free and dp_free
+// let the MMA warp overwrite them with the next step's), and P / dS go to their own
+// columns once the previous step's gradient products are done (pv_done); otherwise P
+// goes over the S columns the warp has read and is signalled on its own (p_half), and
+// dS over the dP columns it has read.
 // KIND 0 (dQ): the row is a query; LSE and D are per row, the mask runs along keys.
 // KIND 1 (dK, dV): the row is a key; LSE and D are per column (query), read from the
 // step's vectors in shared memory (every lane reads the same word), and P^T is
@@ -629,11 +629,20 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
           if (2 * e + 1 >= lim || 2 * e + 1 < lo) pp[e] &= 0x0000FFFFu;
         }
       }
-      // S may now be overwritten by the next step's; with SPLIT, P waits for the previous products
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B.s_free);
-      if (SC::SPLIT && KIND == 1) {
+      if (SC::SPLIT) {  // S may now be overwritten by the next step's
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.s_free);
+      } else {  // P^T over the first half of this warp's S^T columns, read above; then dV may start
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c)
+          tmem_st16(t_p + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pp + 16 * c));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.p_half);
+      }
+      if (SC::SPLIT && KIND == 1) {  // P waits for the previous products
         if (it > 0) {
           if (!(ok = W.wait(B.pv_done, pvd))) break;
           pvd ^= 1;
@@ -676,11 +685,6 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
           if (KIND == 0) pdk[16 * c + e] = pd[e];
         }
         if (KIND == 1) tmem_st16(t_ds + 16 * c, pd);
-      }
-      if (KIND == 1 && !SC::SPLIT) {  // P^T over the second half of this warp's dP^T columns, read above
-#pragma unroll
-        for (int c = 0; c < HC / 32; ++c)
-          tmem_st16(t_p + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pp + 16 * c));
       }
       if (KIND == 1) {  // this warp is done with the step's vectors
         __syncwarp();

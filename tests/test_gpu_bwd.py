@@ -80,10 +80,11 @@ def test_backward_matches_oracle(B, H, T, d, causal):
     _compare(x, do_bits, grads, o, causal, scale, f"T{T} d{d} causal{causal}")
 
 
-@pytest.mark.parametrize("B,H,T,d,causal", [(20, 16, 256, 64, 1), (10, 16, 384, 128, 0)])
+@pytest.mark.parametrize("B,H,T,d,causal", [(20, 16, 256, 64, 1), (10, 16, 384, 128, 0), (8, 16, 512, 128, 1)])
 def test_backward_many_units_per_cta(B, H, T, d, causal):
-    # 640 / 480 units for 152 persistent CTAs: every CTA runs several units, so the
-    # per-step vector buffers and barrier phases carry over from one unit to the next
+    # 640 / 480 / 512 units for 152 persistent CTAs: every CTA runs several units (of
+    # different lengths when causal), so the per-step vector buffers, barrier phases and the
+    # output warps' hand-over (and the next unit's dO at d = 128) carry over between units
     x, do_bits = _inputs(B, H, T, d, seed=53)
     scale = default_scale(d)
     _, grads, o = _run(x, do_bits, causal, scale)
