@@ -498,7 +498,7 @@ def run_sweep(fa, torch, dev, names, peaks, splitkv=SPLITKV_SWEEP, gqa=GQA_SWEEP
         out[f"backward_{name}"] = {"ms_mean": round(sec * 1e3, 4), "tflops": round(f / sec / 1e12, 1),
                                    "pct_of_bf16_peak": round(100 * f / sec / 1e12 / peaks["bf16_tflops"], 1),
                                    "steps": steps, "flops": "2.5 x forward",
-                                   "kernels": "fa_bwd_rowdot_kernel + fa_bwd_kernel (dQ) + fa_bwd_kernel (dK, dV)"}
+                                   "kernels": "fa_bwd_kernel (dQ, with the row vectors) + fa_bwd_kernel (dK, dV)"}
         torch.cuda.empty_cache()
     for name, g in gqa.items():
         f = metric_flops(g["B"], g["H"], g["T"], g["d"], g["causal"])

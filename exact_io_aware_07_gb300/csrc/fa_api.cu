@@ -530,8 +530,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.timeout_ns = kWaitLimitNs;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-  if (fa::launch_bwd_rowdot(d, p, num_sms, stream) != cudaSuccess ||
-      fa::launch_bwd_dq(d, tq, tk, tv, tdo, tdq, tdq, p, grid, stream) != cudaSuccess ||
+  if (fa::launch_bwd_dq(d, tq, tk, tv, tdo, tdq, tdq, p, grid, stream) != cudaSuccess ||
       fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdv, tdk, p, grid, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;

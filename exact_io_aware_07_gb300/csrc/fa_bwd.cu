@@ -6,11 +6,11 @@
 // D_t = sum_c dO_tc O_tc:
 //   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q.
 //
-// Three kernels, no atomics and no T x T matrix in memory:
-//   fa_bwd_rowdot_kernel      D and LSE * log2 e for every row, into a workspace whose rows
-//                             are padded per head to a multiple of 128 (D = 0 and
-//                             LSE * log2 e = +inf there, so P = 0 without a mask);
-//   fa_bwd_kernel<d, 0> (dQ)  per (head, 128-row query tile): stream the key tiles,
+// Two kernels, no atomics and no T x T matrix in memory:
+//   fa_bwd_kernel<d, 0> (dQ)  per (head, 128-row query tile): D and LSE * log2 e of the
+//                             tile's rows into a workspace whose rows are padded per head
+//                             to a multiple of 128 (D = 0 and LSE * log2 e = +inf there,
+//                             so P = 0 without a mask); stream the key tiles,
 //                             S = Q K^T and dP = dO V^T on the tensor core, dS in the
 //                             row warps, dQ += dS K (dS read from Tensor Memory; at
 //                             d = 128 dO is kept in Tensor Memory too);
@@ -32,9 +32,9 @@
 //   warp 9       Tensor Memory allocator and tcgen05.mma issuer (whole warp,
 //                elect.sync picks the issuing lane)
 //   warps 10-13  output warps, one per TMEM lane quarter: the finished unit's
-//                gradients out of Tensor Memory to global memory (and at d = 128 the
-//                dQ kernel's next dO into Tensor Memory) while the row warps start on
-//                the next unit
+//                gradients out of Tensor Memory to global memory while the row warps
+//                start on the next unit; in the dQ kernel also the next unit's D and
+//                LSE * log2 e rows (and at d = 128 its dO into Tensor Memory)
 // Every mbarrier wait is bounded; on expiry the kernel records it in its
 // status word and unwinds, as the forward kernel does.
 #include <cuda.h>
@@ -79,8 +79,8 @@ struct BwdLayout {
   static constexpr int STG_BOX_BYTES = 32 * 64;
   static constexpr int BAR_OFF = STG_OFF + (DIRECT_OUT ? 0 : OUT_WARPS * 2 * STG_BOX_BYTES);
   // res_full, res_empty, ring_full[S], ring_empty[S], s_full, p_full, o_full, o_empty, done, vec_full[2],
-  // s_free, dp_full, dp_free, pv_done, vec_empty[2], do_full, p_half
-  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2 + 1 + 1;
+  // s_free, dp_full, dp_free, pv_done, vec_empty[2], do_full, p_half, rv_full[2]
+  static constexpr int NUM_BARS = 2 + 2 * STAGES + 5 + 2 + 4 + 2 + 1 + 1 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
 };
@@ -120,6 +120,7 @@ struct Bars {
   uint32_t vec_empty;  // [2]: every row warp is done with that vector buffer
   uint32_t do_full;    // the unit's dO is in Tensor Memory (d = 128 dQ kernel)
   uint32_t p_half;     // P^T is written (d = 128 dK/dV kernel)
+  uint32_t rv_full;    // [2]: a unit's D and LSE * log2 e rows are in the workspace (dQ kernel)
 };
 
 template <int D, int KIND>
@@ -144,6 +145,7 @@ __device__ __forceinline__ Bars make_bars(uint32_t base) {
   b.vec_empty = x + 88;
   b.do_full = x + 104;
   b.p_half = x + 112;
+  b.rv_full = x + 120;
   return b;
 }
 
@@ -152,33 +154,28 @@ __device__ __forceinline__ int bwd_unit_of(int k, int b, int G) { return k * G +
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 
-// Over the workspace's padded rows (Tp per head): D_t and LSE_t * log2 e for t < T, 0 and
-// +inf past T.  Each lane reads 16 bytes (8 elements) of O and of dO; D / 8 lanes cover a
-// row, so a warp pass covers 256 / D rows, and each lane keeps four passes' loads in flight.
-// Row numbers fit 32 bits (the host refuses larger shapes), so the head / position split
-// is one 32-bit division.
+// D_t = sum_c dO_tc O_tc and LSE_t * log2 e for the 32 workspace rows [r0, r0 + 32) of head bh
+// (the workspace's rows are padded per head to Tp): D = 0 and LSE * log2 e = +inf past T, so
+// P = 0 there without a mask.  D / 8 lanes cover a row with 16 bytes of O and of dO each, a
+// warp pass covers 256 / D rows, and four passes' loads are issued together.  The stores are
+// plain: the dQ kernel's row warps read the rows after an mbarrier hand-over within the CTA,
+// the dK/dV kernel after this kernel has finished.
 template <int D>
-__global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
-  constexpr int LPR = D / 8;     // lanes per row
-  constexpr int RPW = 32 / LPR;  // rows per warp pass
-  constexpr int U = 4;           // passes per iteration
-  const int lane = threadIdx.x % 32;
-  const uint32_t sub = lane / LPR, part = lane % LPR;
-  const uint32_t rows = static_cast<uint32_t>(p.BH) * static_cast<uint32_t>(p.Tp);
-  const uint32_t Tp = static_cast<uint32_t>(p.Tp), T = static_cast<uint32_t>(p.T);
-  const uint32_t warps = gridDim.x * (blockDim.x / 32);
-  const uint32_t w0 = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  for (uint32_t base = w0 * RPW * U; base < rows; base += warps * RPW * U) {
+__device__ __forceinline__ void bwd_row_vectors(const BwdParams& p, int bh, int r0, int lane) {
+  constexpr int LPR = D / 8;           // lanes per row
+  constexpr int RPW = 32 / LPR;        // rows per warp pass
+  constexpr int PASSES = 32 / RPW, U = 4;  // (eight spill registers)
+  const int sub = lane / LPR, part = lane % LPR;
+  const size_t ws = static_cast<size_t>(bh) * p.Tp;
+#pragma unroll
+  for (int g0 = 0; g0 < PASSES; g0 += U) {
     uint4 a[U], b[U];
-    uint32_t bh[U], t[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint32_t r = base + u * RPW + sub;  // padded row: head r / Tp, position r % Tp
-      bh[u] = r / Tp;
-      t[u] = r - bh[u] * Tp;
+      const int t = r0 + (g0 + u) * RPW + sub;
       a[u] = b[u] = make_uint4(0, 0, 0, 0);
-      if (r < rows && t[u] < T) {
-        const size_t src = static_cast<size_t>(bh[u]) * T + t[u];
+      if (t < p.T) {
+        const size_t src = static_cast<size_t>(bh) * p.T + t;
         a[u] = __ldg(reinterpret_cast<const uint4*>(p.o + src * D) + part);
         b[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + src * D) + part);
       }
@@ -195,11 +192,11 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
         acc = fmaf(xf.y, yf.y, acc);
       }
 #pragma unroll
-      for (int s = LPR / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-      const uint32_t r = base + u * RPW + sub;
-      if (part == 0 && r < rows) {
-        p.drow[r] = acc;  // 0 past T (both rows were read as zeros)
-        p.lse2[r] = t[u] < T ? p.lse[static_cast<size_t>(bh[u]) * T + t[u]] * LOG2E : INFINITY;
+      for (int sh = LPR / 2; sh >= 1; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+      const int t = r0 + (g0 + u) * RPW + sub;
+      if (part == 0) {
+        p.drow[ws + t] = acc;  // 0 past T (both rows were read as zeros)
+        p.lse2[ws + t] = t < p.T ? p.lse[static_cast<size_t>(bh) * p.T + t] * LOG2E : INFINITY;
       }
     }
   }
@@ -234,6 +231,8 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, const Bars& B, uint
     mbar_init(B.pv_done, 1);
     mbar_init(B.do_full, OUT_WARPS);
     mbar_init(B.p_half, ROW_WARPS);
+    mbar_init(B.rv_full, OUT_WARPS);
+    mbar_init(B.rv_full + 8, OUT_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -569,6 +568,7 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
   const int G = gridDim.x;
   uint32_t sf = 0, dpf = 0, pvd = 0;
   int it = 0;  // steps so far (vector buffer, first pv_done wait)
+  int ku = 0;  // dQ kernel: units so far (row-vector hand-over)
   bool ok = true;
   for (int k = 0; ok && k * G < p.num_units; ++k) {
     const int w = bwd_unit_of(k, blockIdx.x, G);
@@ -577,8 +577,11 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
     bwd_decode<KIND>(p, w, bh, rt, first, n);
     const int r0 = rt * BT, row = r0 + r;  // this thread's query (KIND 0) or key (KIND 1)
     const size_t rp = static_cast<size_t>(bh) * p.Tp + row;  // the row in the padded workspace
-    const float lse2_row = KIND == 0 ? p.lse2[rp] : 0.f;      // +inf past T: P = 0 there
-    const float d_row = KIND == 0 ? p.drow[rp] : 0.f;
+    // KIND 0: LSE * log2 e of the row (+inf past T: P = 0 there); D from the output warps,
+    // read once step 0's P has been formed
+    const float lse2_row =
+        KIND == 0 ? (row < p.T ? __ldg(p.lse + static_cast<size_t>(bh) * p.T + row) * LOG2E : INFINITY) : 0.f;
+    float d_row = 0.f;
     for (int t = 0; t < n; ++t, ++it) {
       const int c0 = (first + t) * BT;  // first column of the step: a key (KIND 0) or query (KIND 1)
       const uint32_t lv = vec + ((it & 1) * 2 * BT + HC * h) * 4;  // KIND 1: this half's LSE * log2 e; + 4 BT: D
@@ -651,6 +654,11 @@ __device__ __forceinline__ void bwd_rows(const BwdParams& p, const Waiter& W, co
 #pragma unroll
         for (int c = 0; c < HC / 32; ++c)
           tmem_st16(t_p + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pp + 16 * c));
+      }
+      if (KIND == 0 && t == 0) {  // the output warps have written the unit's D rows
+        if (!(ok = W.wait(B.rv_full + 8 * (ku & 1), (ku >> 1) & 1))) break;
+        ++ku;
+        d_row = __ldcg(p.drow + rp);
       }
       if (!(ok = W.wait(B.dp_full, dpf))) break;
       dpf ^= 1;
@@ -765,19 +773,34 @@ __device__ __forceinline__ void bwd_out(const BwdParams& p, const Waiter& W, con
     __syncwarp();
     if (lane == 0) mbar_arrive(B.do_full);
   };
+  auto put_rv = [&](int k, int b) {  // dQ kernel: unit k's D and LSE * log2 e rows, then rv_full[b]
+    // (the row warps wait for D only once step 0's P is formed; the dK/dV kernel reads both)
+    int bh, rt, first, n;
+    bwd_decode<KIND>(p, bwd_unit_of(k, blockIdx.x, G), bh, rt, first, n);
+    bwd_row_vectors<D>(p, bh, rt * BT + q4 * 32, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.rv_full + 8 * b);
+  };
   uint32_t of = 0;
   bool ok = true;
   int nb = 0;             // boxes staged so far: the next goes to staging box nb & 1
   bool stg_busy = false;  // a TMA store may still be reading a staging box
-  if (L::DO_TMEM) {
+  int ku = 0;             // units so far
+  {
     const int k0 = next_unit(0);
-    if (k0 >= 0) put_do(k0);
+    if (KIND == 0 && k0 >= 0) put_rv(k0, 0);
+    if (L::DO_TMEM && k0 >= 0) put_do(k0);
   }
   for (int k = 0; ok && k * G < p.num_units; ++k) {
     const int w = bwd_unit_of(k, blockIdx.x, G);
     if (w >= p.num_units) continue;
     int bh, rt, first, n;
     bwd_decode<KIND>(p, w, bh, rt, first, n);
+    if (KIND == 0) {  // the next unit's vectors while this one runs
+      const int k2 = next_unit(k + 1);
+      if (k2 >= 0) put_rv(k2, (ku + 1) & 1);
+    }
+    ++ku;
     if (!(ok = W.wait(B.o_full, of))) break;
     of ^= 1;
     tc_fence_after();
@@ -929,18 +952,6 @@ cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 }
 
 }  // namespace
-
-cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream) {
-  const size_t rows = static_cast<size_t>(p.BH) * p.Tp;
-  const size_t per_block = static_cast<size_t>(8) * (256 / d) * 4;  // warps x rows per pass x passes
-  const size_t blocks = (rows + per_block - 1) / per_block;
-  const int grid = static_cast<int>(blocks < static_cast<size_t>(num_sms) * 8 ? blocks : num_sms * 8);
-  if (d == 64)
-    fa_bwd_rowdot_kernel<64><<<grid, 256, 0, stream>>>(p);
-  else
-    fa_bwd_rowdot_kernel<128><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& dout, const CUtensorMap& g1, const CUtensorMap& g2, const BwdParams& p,

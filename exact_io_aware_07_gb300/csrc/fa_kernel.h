@@ -88,7 +88,6 @@ struct BwdParams {
 };
 
 // D_t = sum_c dO_tc O_tc and LSE_t * log2 e for every row of the padded workspace.
-cudaError_t launch_bwd_rowdot(int d, const BwdParams& p, int num_sms, cudaStream_t stream);
 // dQ: one CTA per SM, units (head, 128-row query tile), key tiles streamed.
 // Gradient outputs (dQ, dK, dV: bf16 (d, T, B*H), no swizzle) are written in boxes of
 // kGradBoxRows rows x kGradBoxCols columns: a row warp's 32 rows and 32 of its columns.
