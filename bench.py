@@ -412,7 +412,7 @@ BWD_SWEEP = ["gpt2s_causal_b8h12t1024d64", "llama8b_causal_b1h32t4096d128", "lla
 
 
 def time_bwd(fa, torch, dev, w, steps):
-    """Device time of fa_bwd (three kernels) per step, inputs rotating past L2."""
+    """Device time of fa_bwd (both kernels) per step, inputs rotating past L2."""
     B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
     qkv = fi.make_qkv(B, H, T, d, seed=0, sigma_qk=w["sigma_qk"])
     q0, k0, v0 = device_inputs(qkv, torch, dev)
