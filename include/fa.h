@@ -193,13 +193,15 @@ size_t fa_fwd_fp8_workspace_bytes(int B, int H, int T, int d);
  *   workspace        : device memory of at least fa_bwd_workspace_bytes(B, H, T)
  *                      bytes, 16-byte aligned (it receives D and LSE * log2 e per
  *                      row; nothing in it needs to be set beforehand).
- * Three kernels run in order on `stream`: D, then dQ (one unit per 128-row query
- * tile), then dK and dV (one unit per 128-key tile); no output is accumulated
- * across units, so the result does not depend on scheduling.
+ * Two kernels run in order on `stream`: dQ (one unit per 128-row query tile,
+ * which also writes D and LSE * log2 e into the workspace), then dK and dV (one
+ * unit per 128-key tile, reading them); no output is accumulated across units,
+ * so the result does not depend on scheduling.
  * Errors: as fa_fwd for the shared arguments; FA_ERR_NULL_PTR / FA_ERR_MISALIGNED
  * / FA_ERR_BAD_POINTER for dout, dq, dk, dv; FA_ERR_WORKSPACE for a NULL or too
  * small workspace; FA_ERR_ALIAS when an output or the workspace overlaps an input
- * or another output.
+ * or another output; FA_ERR_BAD_SHAPE when B * H * (T rounded up to 128) exceeds
+ * 2^31 - 1.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dout, void* dq, void* dk, void* dv,
