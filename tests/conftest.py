@@ -25,3 +25,14 @@ def load_golden(name):
 @pytest.fixture
 def golden():
     return load_golden
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Prints the literal errors of every GPU-vs-oracle comparison this session made."""
+    parity = sys.modules.get("parity")
+    records = getattr(parity, "RECORDS", None) if parity else None
+    if not records:
+        return
+    terminalreporter.section("parity against the float64 oracle")
+    for label, rec in records:
+        terminalreporter.write_line(parity.format_record(label, rec))

@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 import fa_inputs as fi
-from parity import bf16_to_f64, bwd_bounds, default_scale, to_device
+from parity import bf16_to_f64, bwd_bounds, default_scale, record, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +59,7 @@ def _compare(x, do_bits, grads, o_gpu, causal, scale, label):
     q, k, v = x.f64("q"), x.f64("k"), x.f64("v")
     do = fi.bf16_bits_to_f64(do_bits).reshape(q.shape)
     B, H = q.shape[:2]
+    worst = {n: [0.0, 0.0] for n in ("dQ", "dK", "dV")}  # max |err|, max |err| / bound
     for b in range(B):
         for h in range(H):
             refs, bounds = bwd_bounds(q[b, h], k[b, h], v[b, h], do[b, h], o_gpu[b, h], bool(causal), scale)
@@ -67,6 +68,10 @@ def _compare(x, do_bits, grads, o_gpu, causal, scale, label):
                 bad = ~(err <= bound)  # NaN counts as bad
                 assert not bad.any(), (f"{label} {name} b{b} h{h}: {int(bad.sum())} of {bad.size} elements outside "
                                        f"the bound; max err {float(np.nanmax(err)):.3g}")
+                worst[name][0] = max(worst[name][0], float(err.max()))
+                worst[name][1] = max(worst[name][1], float((err / bound).max()))
+    record(f"backward {label}", {f"max|{n}| err": w[0] for n, w in worst.items()}
+           | {f"{n} err/bound": w[1] for n, w in worst.items()})
 
 
 @pytest.mark.parametrize("B,H,T,d,causal", [
@@ -89,6 +94,17 @@ def test_backward_many_units_per_cta(B, H, T, d, causal):
     scale = default_scale(d)
     _, grads, o = _run(x, do_bits, causal, scale)
     _compare(x, do_bits, grads, o, causal, scale, f"B{B} H{H} T{T} d{d} causal{causal}")
+
+
+@pytest.mark.parametrize("causal", [1, 0])
+def test_backward_llama8b_size(causal):
+    # the size the backward is timed at: Llama-3.1-8B attention, 32 heads, T = 4096, d = 128
+    # (1,024 units per kernel); the float64 oracle runs one head at a time
+    B, H, T, d = 1, 32, 4096, 128
+    x, do_bits = _inputs(B, H, T, d, seed=0)
+    scale = default_scale(d)
+    _, grads, o = _run(x, do_bits, causal, scale)
+    _compare(x, do_bits, grads, o, causal, scale, f"llama8b B1 H32 T4096 d128 causal{causal}")
 
 
 def test_backward_outputs_exactly_covered():

@@ -10,7 +10,7 @@ import time
 import pytest
 
 import fa_inputs as fi
-from parity import compare, default_scale, run_gpu
+from parity import compare, default_scale, rounding_bound, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -36,5 +36,6 @@ def test_bounded_wait_times_out_and_reports():
 
     qkv = fi.make_qkv(1, 2, 300, 64, seed=12)
     o, lse = run_gpu(qkv, True, default_scale(64))
-    O_ref, lse_ref = oracle.attention_fwd(qkv.f64("q"), qkv.f64("k"), qkv.f64("v"), True, default_scale(64))
-    compare(o, lse, O_ref, lse_ref, label="after timeout")
+    q64, k64, v64 = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    O_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, True, default_scale(64))
+    compare(o, lse, O_ref, lse_ref, label="after timeout", bound=rounding_bound(q64, k64, v64, True, default_scale(64)))

@@ -25,7 +25,7 @@ import pytest
 
 import fa_inputs as fi
 import oracle.attention as A
-from parity import bf16_to_f64
+from parity import bf16_to_f64, record
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +59,7 @@ def _run(x, causal, scale):
 def _check(x, o, lse, causal, scale, label):
     q, k, v = x.f64("q"), x.f64("k"), x.f64("v")
     worst_mean = 0.0
+    worst_ratio = worst_abs = worst_lse = 0.0
     for b in range(x.B):
         for h in range(x.H):
             S = A.scores(q[b, h], k[b, h], scale)
@@ -75,9 +76,15 @@ def _check(x, o, lse, causal, scale, label):
             err = np.abs(o[b, h] - O_ref)
             bad = ~(err <= bound)
             assert not bad.any(), f"{label} b{b} h{h}: {int(bad.sum())} elements outside the bound, max {np.nanmax(err):.3g}"
-            assert np.abs(lse[b, h] - lse_ref).max() <= 1e-3, f"{label} b{b} h{h}: LSE"
+            lerr = float(np.abs(lse[b, h] - lse_ref).max())
+            assert lerr <= 1e-3, f"{label} b{b} h{h}: LSE"
             worst_mean = max(worst_mean, float(err.mean() / wv.mean()))
+            worst_ratio = max(worst_ratio, float((err / bound).max()))
+            worst_abs = max(worst_abs, float(err.max()))
+            worst_lse = max(worst_lse, lerr)
     assert worst_mean <= 2.0 ** -6, f"{label}: mean error {worst_mean:.3g} of the mean weighted |v|"
+    record(label, {"max|dO|": worst_abs, "max err/bound": worst_ratio, "mean err / mean sum w|v|": worst_mean,
+                   "max|dLSE|": worst_lse})
 
 
 @pytest.mark.parametrize("B,H,T,causal", [(1, 2, 128, 0), (1, 2, 300, 1), (2, 2, 1000, 0), (1, 3, 17, 1),
@@ -87,6 +94,15 @@ def test_fp8_matches_oracle(B, H, T, causal):
     scale = 128 ** -0.5
     o, lse = _run(x, causal, scale)
     _check(x, o, lse, causal, scale, f"fp8 T{T} causal{causal}")
+
+
+@pytest.mark.parametrize("causal", [1, 0])
+def test_fp8_llama8b_size(causal):
+    # the size the e4m3 forward is timed at: 32 heads, T = 4096, d = 128
+    x = fi.make_qkv_e4m3(1, 32, 4096, 128, seed=0)
+    scale = 128 ** -0.5
+    o, lse = _run(x, causal, scale)
+    _check(x, o, lse, causal, scale, f"fp8 llama8b B1 H32 T4096 causal{causal}")
 
 
 def test_fp8_scales():

@@ -10,7 +10,7 @@ import pytest
 
 import fa_inputs as fi
 import oracle
-from parity import bf16_to_f64, compare, default_scale, to_device
+from parity import bf16_to_f64, compare, default_scale, rounding_bound, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -48,9 +48,11 @@ def test_gqa_matches_oracle(B, H, Hkv, T, d, causal):
     x = fi.make_grouped_qkv(B, H, Hkv, T, d, seed=41)
     scale = default_scale(d)
     _, _, _, o, lse = _run(x, causal, scale)
-    O_ref, lse_ref = oracle.attention_fwd_gqa(x.f64("q"), x.f64("k"), x.f64("v"), causal, scale)
+    q64, k64, v64 = x.f64("q"), x.f64("k"), x.f64("v")
+    O_ref, lse_ref = oracle.attention_fwd_gqa(q64, k64, v64, causal, scale)
     compare(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O_ref, lse_ref,
-            label=f"gqa B{B} H{H} Hkv{Hkv} T{T} d{d} causal{causal}")
+            label=f"gqa B{B} H{H} Hkv{Hkv} T{T} d{d} causal{causal}",
+            bound=rounding_bound(q64, k64, v64, causal, scale))
 
 
 @pytest.mark.parametrize("d,causal", [(64, 1), (128, 0)])

@@ -12,7 +12,7 @@ import pytest
 
 import fa_inputs as fi
 import oracle
-from parity import bf16_to_f64, compare, default_scale, to_device
+from parity import bf16_to_f64, compare, default_scale, rounding_bound, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -78,8 +78,10 @@ def test_paged_matches_contiguous(B, H, Hkv, T, d, causal):
     scale = default_scale(d)
     q, o, lse = _run(x, kp, vp, table, causal, scale)
     assert fa.fa_device_status() == 0
-    O_ref, lse_ref = oracle.attention_fwd_gqa(x.f64("q"), x.f64("k"), x.f64("v"), causal, scale)
-    compare(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O_ref, lse_ref, label=f"paged T{T} d{d}")
+    q64, k64, v64 = x.f64("q"), x.f64("k"), x.f64("v")
+    O_ref, lse_ref = oracle.attention_fwd_gqa(q64, k64, v64, causal, scale)
+    compare(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O_ref, lse_ref, label=f"paged T{T} d{d}",
+            bound=rounding_bound(q64, k64, v64, causal, scale))
     k, v = to_device(None, x.k_bits), to_device(None, x.v_bits)
     o2, lse2 = fa.attention_gqa(q, k, v, causal=bool(causal), scale=scale)
     torch.cuda.synchronize()

@@ -10,7 +10,7 @@ import pytest
 
 import fa_inputs as fi
 import oracle
-from parity import compare, default_scale, run_gpu, sampled_rows, to_device
+from parity import compare, default_scale, rounding_bound, run_gpu, sampled_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -26,14 +26,16 @@ def _library():
     fa.load_library()
 
 
-def _check(B, H, T, d, causal, seed=1, sigma_qk=1.0, scale=None, rows=None):
+def _check(B, H, T, d, causal, seed=1, sigma_qk=1.0, scale=None, rows=None, label=None):
     qkv = fi.make_qkv(B, H, T, d, seed=seed, sigma_qk=sigma_qk)
     scale = default_scale(d) if scale is None else scale
     o, lse = run_gpu(qkv, causal, scale)
     if rows is not None:
         o, lse = o[:, :, rows], lse[:, :, rows]
-    O_ref, lse_ref = oracle.attention_fwd(qkv.f64("q"), qkv.f64("k"), qkv.f64("v"), causal, scale, rows=rows)
-    return compare(o, lse, O_ref, lse_ref, label=f"B{B} H{H} T{T} d{d} causal{causal}")
+    q64, k64, v64 = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    O_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, causal, scale, rows=rows)
+    label = label or f"B{B} H{H} T{T} d{d} causal{causal} seed{seed}"
+    return compare(o, lse, O_ref, lse_ref, label=label, bound=rounding_bound(q64, k64, v64, causal, scale, rows))
 
 
 # ragged and tiny sequence lengths: one tile, several tiles, a ragged tail, a lone
@@ -69,24 +71,26 @@ def test_three_token_example_padded():
     assert np.allclose(lse[0, 0].cpu().numpy(), np.log([1.0, 2.0, 3.0]), atol=1e-6)
 
 
-@pytest.mark.parametrize("name,seeds", [
-    ("tiny_causal_b1h4t256d64", (0, 1, 2)),
-    ("gpt2s_causal_b8h12t1024d64", (0, 1, 2)),
-    ("gpt2m_b16h16t1024d64", (0,)),
-    ("gpt2m_stress_b16h16t1024d64", (0,)),
-    ("llama8b_causal_b1h32t4096d128", (0,)),
-    ("llama8b_b1h32t4096d128", (0,)),
+@pytest.mark.parametrize("name", [
+    "tiny_causal_b1h4t256d64",
+    "gpt2s_causal_b8h12t1024d64",
+    "gpt2m_b16h16t1024d64",
+    "gpt2m_stress_b16h16t1024d64",
+    "llama8b_causal_b1h32t4096d128",
+    "llama8b_b1h32t4096d128",
 ])
-def test_workload_full(name, seeds):
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_workload_full(name, seed):
     w = fi.WORKLOADS[name]
-    for seed in seeds:
-        _check(w["B"], w["H"], w["T"], w["d"], w["causal"], seed=seed, sigma_qk=w["sigma_qk"])
+    _check(w["B"], w["H"], w["T"], w["d"], w["causal"], seed=seed, sigma_qk=w["sigma_qk"],
+           label=f"{name} seed{seed}")
 
 
 def test_long_context_sampled_rows():
     w = fi.WORKLOADS["long_causal_b1h32t32768d128"]
     rows = sampled_rows(w["T"], seed=7)
-    _check(w["B"], w["H"], w["T"], w["d"], w["causal"], seed=0, rows=rows)
+    _check(w["B"], w["H"], w["T"], w["d"], w["causal"], seed=0, rows=rows,
+           label=f"long_causal_b1h32t32768d128 seed0 ({rows.size} sampled rows per head)")
 
 
 def test_many_units_per_cta():

@@ -8,7 +8,7 @@ import pytest
 
 import fa_inputs as fi
 import oracle
-from parity import bf16_to_f64, compare, default_scale, to_device
+from parity import bf16_to_f64, compare, default_scale, rounding_bound, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -49,8 +49,10 @@ def test_splitkv_matches_oracle(T, num_splits, d, causal):
     qkv = fi.make_qkv(1, 3, T, d, seed=21)
     scale = default_scale(d)
     o, lse = _run_split(qkv, causal, scale, num_splits)
-    O_ref, lse_ref = oracle.attention_fwd(qkv.f64("q"), qkv.f64("k"), qkv.f64("v"), causal, scale)
-    compare(o, lse, O_ref, lse_ref, label=f"split{num_splits} T{T} d{d} causal{causal}")
+    q64, k64, v64 = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    O_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, causal, scale)
+    compare(o, lse, O_ref, lse_ref, label=f"split{num_splits} T{T} d{d} causal{causal}",
+            bound=rounding_bound(q64, k64, v64, causal, scale))
 
 
 @pytest.mark.parametrize("name,num_splits", [("tiny_causal_b1h4t256d64", 2), ("gpt2s_causal_b8h12t1024d64", 4),
@@ -60,8 +62,10 @@ def test_splitkv_workloads(name, num_splits):
     qkv = fi.make_qkv(w["B"], w["H"], w["T"], w["d"], seed=0, sigma_qk=w["sigma_qk"])
     scale = default_scale(w["d"])
     o, lse = _run_split(qkv, w["causal"], scale, num_splits)
-    O_ref, lse_ref = oracle.attention_fwd(qkv.f64("q"), qkv.f64("k"), qkv.f64("v"), w["causal"], scale)
-    compare(o, lse, O_ref, lse_ref, label=f"{name} split{num_splits}")
+    q64, k64, v64 = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    O_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, w["causal"], scale)
+    compare(o, lse, O_ref, lse_ref, label=f"{name} split{num_splits}",
+            bound=rounding_bound(q64, k64, v64, w["causal"], scale))
 
 
 def test_splitkv_rejects_bad_workspace():
