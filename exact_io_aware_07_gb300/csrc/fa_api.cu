@@ -235,6 +235,7 @@ fa_status prepare(const void* q, const void* k, const void* v, void* o, float* l
   p.nqb = (T + 255) / 256;
   p.nk = (T + 127) / 128;
   p.num_units = BH * p.nqb;
+  p.unit_div = causal ? BH : p.nqb;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.v_descale = 1.f;
   p.timeout_ns = kWaitLimitNs;
@@ -340,6 +341,7 @@ fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, 
   p.nqb = (T + 255) / 256;
   p.nk = nk;
   p.num_units = BH * p.nqb;
+  p.unit_div = causal ? BH : p.nqb;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.v_descale = 1.f;
   p.timeout_ns = kWaitLimitNs;
@@ -361,7 +363,7 @@ fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, vo
   if (st != FA_OK) return st;
   if (fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (fa::noalloc_scratch_address(pr.dev, &scratch) != cudaSuccess) {
+  if (fa::noalloc_scratch_address(&scratch) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }
@@ -451,6 +453,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
   p.nqb = (T + 255) / 256;
   p.nk = (T + 127) / 128;
   p.num_units = BH * p.nqb;
+  p.unit_div = causal ? BH : p.nqb;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * q_descale * k_descale * 1.4426950408889634074);
   p.v_descale = v_descale;
   p.timeout_ns = kWaitLimitNs;

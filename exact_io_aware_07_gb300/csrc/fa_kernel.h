@@ -23,6 +23,7 @@ struct Params {
   int nqb;                    // 256-row query blocks per head: ceil(T / 256)
   int nk;                     // 128-key tiles per head: ceil(T / 128)
   int num_units;              // BH * nqb
+  int unit_div;               // causal: BH (units listed band by band); otherwise nqb (head by head)
   float scale_log2;           // scale * log2(e) (e4m3: times the Q and K scales)
   float v_descale;            // 1, or the scale of e4m3 V (the real value is the byte's value times it)
   unsigned long long timeout_ns;  // bound on every in-kernel wait
@@ -60,9 +61,9 @@ cudaError_t measure_ex2_rate(int num_sms, double* ops_per_second, cudaStream_t s
 
 // Size of the fixed device scratch behind fa_fwd_splitkv_noalloc (32 MiB).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
-// Device address of that scratch on device `dev` (must be the current device);
-// looked up on the first call for each device, then cached.
-cudaError_t noalloc_scratch_address(int dev, void** out);
+// Device address of that scratch in the current CUDA context; looked up on the first
+// call in each context (cudaGetSymbolAddress), then cached by the context's unique id.
+cudaError_t noalloc_scratch_address(void** out);
 
 // ---------------------------------------------------------------- backward pass (fa_bwd.cu)
 

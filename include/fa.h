@@ -233,7 +233,11 @@ size_t fa_bwd_workspace_bytes(int B, int H, int T);
  *     FA_NOALLOC_SCRATCH_BYTES, else FA_ERR_WORKSPACE and nothing runs;
  *   - the first call on each device looks up the scratch's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture on that device;
+ *     that first call before any stream capture on that device.  The
+ *     address belongs to the CUDA context that was current: after a
+ *     cudaDeviceReset, or when a driver-API caller makes another context
+ *     current, the next call looks it up again (the cache is keyed on the
+ *     context's unique id), and that call too should precede any capture;
  *   - every call on a device shares the one scratch array, which keeps what
  *     the last call left there.  Nothing in it needs to start at zero: each
  *     call writes every partial before its merge reads it.  Calls whose

@@ -4,10 +4,15 @@ fa_fwd_splitkv_noalloc is for callers that cannot allocate device memory while
 they run (their memory belongs to a framework pool or a fixed budget, or the
 allocator must not be called at that point).  It keeps its split partials in a
 fixed scratch array the library holds on each device, so it takes only inputs
-and outputs.  This test checks that two calls in a row, on different inputs,
-give what fa_fwd_splitkv gives with a caller-provided workspace, within the
-parity tolerances used for every GPU result here, and that a problem whose
-partials would not fit the fixed scratch is refused.
+and outputs.
+
+This test issues two calls back to back on one stream, on different inputs and
+shapes, and synchronises once: the second call reuses the scratch the first
+one wrote, so stream order alone must keep them apart.  Each output must equal
+fa_fwd_splitkv's (same kernels, same split count, a caller-provided workspace)
+bit for bit, and must match the float64 oracle within the parity tolerances
+used for every GPU result here.  A problem whose partials would not fit the
+fixed scratch is refused before anything is launched.
 
 The file name sorts last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
@@ -18,7 +23,8 @@ import numpy as np
 import pytest
 
 import fa_inputs as fi
-from parity import bf16_to_f64, compare, default_scale, to_device
+import oracle
+from parity import bf16_to_f64, compare, default_scale, rounding_bound, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +38,7 @@ def _noalloc(lib, q, k, v, o, lse, causal, scale, num_splits):
                                       B, H, T, d, int(causal), ctypes.c_float(scale), num_splits, st)
 
 
-def test_noalloc_matches_workspace_version_twice():
+def test_noalloc_two_calls_in_a_row():
     import torch
 
     import exact_io_aware_07_gb300 as fa
@@ -44,19 +50,31 @@ def test_noalloc_matches_workspace_version_twice():
         (fi.make_qkv(2, 3, 1000, 128, seed=31), True, 3),
         (fi.make_qkv(1, 4, 777, 64, seed=32, sigma_qk=2.0), False, 2),
     ]
+    runs = []
     for qkv, causal, ns in cases:
         q, k, v = (to_device(None, b) for b in (qkv.q_bits, qkv.k_bits, qkv.v_bits))
         B, H, T, d = q.shape
-        scale = default_scale(d)
         assert fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, ns) <= fa.FA_NOALLOC_SCRATCH_BYTES
-        o_ref, lse_ref = fa.attention_splitkv(q, k, v, causal=causal, num_splits=ns, scale=scale)
         o = torch.full_like(q, float("nan"))
         lse = torch.full((B, H, T), float("nan"), dtype=torch.float32, device="cuda")
-        assert _noalloc(lib, q, k, v, o, lse, causal, scale, ns) == 0
+        runs.append((qkv, causal, ns, q, k, v, o, lse))
+    torch.cuda.synchronize()
+    for qkv, causal, ns, q, k, v, o, lse in runs:  # no synchronisation between the calls
+        assert _noalloc(lib, q, k, v, o, lse, causal, default_scale(q.shape[3]), ns) == 0
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for qkv, causal, ns, q, k, v, o, lse in runs:
+        B, H, T, d = q.shape
+        scale = default_scale(d)
+        o_ws, lse_ws = fa.attention_splitkv(q, k, v, causal=causal, num_splits=ns, scale=scale)
         torch.cuda.synchronize()
-        assert fa.fa_device_status() == 0
-        compare(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64),
-                bf16_to_f64(o_ref), lse_ref.cpu().numpy().astype(np.float64), label=f"noalloc T{T} d{d}")
+        assert torch.equal(o.view(torch.int16), o_ws.view(torch.int16)), f"T{T} d{d}: O differs from fa_fwd_splitkv"
+        assert torch.equal(lse, lse_ws), f"T{T} d{d}: LSE differs from fa_fwd_splitkv"
+        q64, k64, v64 = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+        O_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, causal, scale)
+        compare(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O_ref, lse_ref,
+                label=f"noalloc split{ns} B{B} H{H} T{T} d{d} causal{int(causal)}",
+                bound=rounding_bound(q64, k64, v64, causal, scale))
 
 
 def test_noalloc_refuses_problems_beyond_the_fixed_scratch():
