@@ -79,10 +79,14 @@ struct Layout {
   static constexpr int STAGES = (D == 128 && !F8) ? 4 : 6;     // K/V ring depth (tiles)
   static constexpr int Q_OFF = 0;                      // [QBUF units][2 query tiles]
   static constexpr int KV_OFF = QBUF * 2 * TILE_BYTES;
-  // d = 64: P_i has Tensor Memory columns of its own, so S_i(j+1) may be computed
+  // d = 64: P_i has Tensor Memory columns of its own, so the next S may be computed
   // while the softmax of S_i(j) runs (see the MMA issuer); d = 128: P_i overwrites S_i.
   static constexpr bool SEP_P = (D == 64) && !F8;
+  // d = 64: O_i += P_i [V_j | 1]: the P V product also forms the sum of the rounded weights
+  // (16 columns of ones after V, read from a constant block in shared memory), which divides O.
+  static constexpr bool ONES = SEP_P;
   static constexpr int ON = D;                          // O columns per query tile in TMEM
+  static constexpr int ON_MMA = ONES ? D + 16 : D;      // columns the P V product writes
   // d = 64: one MMA-issuing warp per query tile (warps 9, 10; warp 11 idle); d = 128: warp 9 alone
   static constexpr int THREADS = SEP_P ? 384 : 320;
   static constexpr int MMA_WARPS = SEP_P ? 2 : 1;
@@ -92,20 +96,29 @@ struct Layout {
   static constexpr int STG_OFF = KV_OFF + STAGES * TILE_BYTES;
   static constexpr bool STG2 = F8;
   static constexpr int STG_WARP_BYTES = (STG2 ? 2 : 1) * 32 * 128;
-  static constexpr int BAR_OFF = STG_OFF + 8 * STG_WARP_BYTES;
+  // d = 64: the ones block, laid out as one more 64-column V atom (128 rows of 128 bytes, 1 KB aligned)
+  static constexpr int ONES_OFF = STG_OFF + 8 * STG_WARP_BYTES;
+  static constexpr int ONES_BYTES = ONES ? 128 * 128 : 0;
+  static constexpr int BAR_OFF = ONES_OFF + ONES_BYTES;
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2],
   // s_free[2], done
   static constexpr int NUM_BARS = 4 + 2 * STAGES + 10 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // TMEM base slot, abort flag
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
-  static __device__ __forceinline__ constexpr uint32_t s_col(int i) { return uint32_t(i) * 128u; }
-  static __device__ __forceinline__ constexpr uint32_t o_col(int i) { return 256u + uint32_t(i) * ON; }
-  // where P_i lives: its own 64 columns after O_1, or the first 64 columns of S_i
+  // Tensor Memory columns.  d = 128 and e4m3: S_0 [0,128), S_1 [128,256), O_0, O_1 after them, P_i
+  // over S_i.  d = 64: one S buffer [0,128) that the two query tiles' products take in turn,
+  // O_0 [128,208) and O_1 [224,304) (64 columns of O and 16 of the weight sum each),
+  // P_0 [320,384) and P_1 [384,448).
+  static __device__ __forceinline__ constexpr uint32_t s_col(int i) { return SEP_P ? 0u : uint32_t(i) * 128u; }
+  static __device__ __forceinline__ constexpr uint32_t o_col(int i) {
+    return SEP_P ? 128u + uint32_t(i) * 96u : 256u + uint32_t(i) * ON;
+  }
   static __device__ __forceinline__ constexpr uint32_t p_col(int i) {
-    return SEP_P ? 256u + 2u * ON + uint32_t(i) * 64u : s_col(i);
+    return SEP_P ? 320u + uint32_t(i) * 64u : s_col(i);
   }
 };
-static_assert(!Layout<64>::SEP_P || 256 + 2 * Layout<64>::ON + 128 <= 512, "Tensor Memory columns exceed 512");
+static_assert(Layout<64>::ON_MMA <= 96 && 320 + 2 * 64 <= 512, "Tensor Memory columns exceed 512");
+static_assert(Layout<64>::ONES_OFF % 1024 == 0, "the ones block must be 1 KB aligned like the V tiles");
 
 constexpr int MAX_SMEM_PER_CTA = 232448;  // 227 KB opt-in dynamic shared memory per block on sm_103
 static_assert(Layout<64>::SMEM_BYTES <= MAX_SMEM_PER_CTA && Layout<128>::SMEM_BYTES <= MAX_SMEM_PER_CTA,
@@ -119,9 +132,12 @@ struct Unit {
 };
 
 // Work item w -> (batch*head, 256-row query block[, key split]).  Causal
-// launches list the longest query blocks first.  With split keys, split s of a
-// unit covers key tiles [s * split_tiles, (s + 1) * split_tiles) of what each
-// query tile may see.
+// launches list the longest query blocks first (all heads' longest blocks, then
+// the next longest, ...), which balances the persistent CTAs.  Non-causal units
+// all cost the same, so they are listed head by head: the CTAs running at one
+// time then share a few heads' K and V, which stay in L2.  With split keys,
+// split s of a unit covers key tiles [s * split_tiles, (s + 1) * split_tiles)
+// of what each query tile may see.
 template <bool PARTIAL>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
   Unit u;
@@ -132,9 +148,10 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
     const int rem = w - band * per_band;
     s = rem / p.BH;
     u.bh = rem - s * p.BH;
-  } else {
-    band = w / p.BH;
-    u.bh = w - band * p.BH;
+  } else {  // one division: w = first * unit_div + second
+    const int first = w / p.unit_div, second = w - first * p.unit_div;
+    band = p.causal ? first : second;
+    u.bh = p.causal ? second : first;
   }
   u.qb = p.causal ? (p.nqb - 1 - band) : band;
   const int q0 = u.qb * 2 * BM, q1 = q0 + BM;
@@ -229,6 +246,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (warp == MMA_WARP0) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
+  }
+  if (L::ONES) {  // bf16 1.0 everywhere in the block; the tensor core reads it through the async proxy
+    for (int t = threadIdx.x; t < L::ONES_BYTES / 16; t += L::THREADS)
+      st_shared_v4(sbase + L::ONES_OFF + 16 * t, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -375,23 +397,32 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // warps walk the whole K/V ring in the producer's order and release every stage (and
     // the unit's Q buffer) whether or not their tile used it, so kv_empty and q_empty
     // complete after two arrivals.
+    //
+    // The two tiles' S products share one Tensor Memory buffer and take it in turn: per K/V
+    // step S_0(x), then S_1(x) (a tile past its last step drops out), unit after unit.  A
+    // product is issued once the softmax has read the one before it in that order, which
+    // s_free[t] reports for tile t (it completes once per S_t read).  Because the products
+    // are strictly ordered, the awaited completion is always the next one of that barrier.
     {
       const int i = warp - MMA_WARP0;  // query tile of this warp
-      constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);   // S = Q K^T: both K-major
-      constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, L::ON, 1);  // O += P V: V is MN-major
-      // Descriptor halves: the address field (low 14 bits, in 16-byte units) is the
-      // only part that changes, and every offset added below stays inside it.
+      constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);          // S = Q K^T: both K-major
+      constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, L::ON_MMA, 1);  // O += P [V | 1]: V is MN-major
+      // Descriptor halves: the address field (low 14 bits, in 16-byte units) and, for V, the
+      // leading byte offset (bits 16-29: from the V tile to the ones block, the second 64-column
+      // atom of B) are the parts that change; every offset added below stays inside its field.
       const uint64_t dqk = make_sdesc_sw128(sbase, 16, 1024);        // K-major tiles (Q, K)
       const uint64_t dvv = make_sdesc_sw128(sbase, BOX_BYTES, 1024);  // MN-major V tiles
       const uint32_t dqk_lo = uint32_t(dqk), dqk_hi = uint32_t(dqk >> 32);
-      const uint32_t dv_lo = uint32_t(dvv), dv_hi = uint32_t(dvv >> 32);
-      const uint32_t my_s_full = bar_s_full + 8 * i, my_p_full = bar_p_full + 8 * i;
+      const uint32_t dv_hi = uint32_t(dvv >> 32);
+      const uint32_t ones_addr = sbase + L::ONES_OFF;
+      const uint32_t my_p_full = bar_p_full + 8 * i;
       const uint32_t my_o_full = bar_o_full + 8 * i, my_o_empty = bar_o_empty + 8 * i;
-      const uint32_t my_s_free = bar_s_free + 8 * i;
       const uint32_t d_s = tmem + L::s_col(i), d_o = tmem + L::o_col(i), a_p = tmem + L::p_col(i);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t pf = 0, oe = 0, sfr = 0;
+      uint32_t pf = 0, oe = 0;
+      int cnt0 = 0, cnt1 = 0;  // S products of tile 0 / tile 1 in the units before this one
+      int last_t = -1;         // tile of the last S product of those units (-1: none yet)
       bool ok = true;
       int nu = 0;
       int bal = 0;
@@ -407,23 +438,36 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         ++nu;
         tc_fence_after();
         const uint32_t a_q = dqk_lo + ((L::Q_OFF + (2 * qb + i) * L::TILE_BYTES) >> 4);
-        // S_i = Q_i K^T over d in steps of 16 (stage ks of the ring); after the tile's last S
-        // the Q buffer is released
+        // S_i(x) over d in steps of 16 (stage ks of the ring), after the S product before it has been
+        // read; after the tile's last S the Q buffer is released
 #define FA_ISSUE_S(ks, x)                                                                               \
   {                                                                                                     \
+    int pt = -1, pk = 0; /* tile and per-tile index of the S product before S_i(x) */                   \
+    if (i == 1 && (x) < u.n0) {                                                                         \
+      pt = 0, pk = cnt0 + (x);                                                                          \
+    } else if ((x) > 0) {                                                                               \
+      if (i == 0 && (x) - 1 < u.n1) pt = 1, pk = cnt1 + (x) - 1;                                        \
+      else pt = i, pk = (i ? cnt1 : cnt0) + (x) - 1;                                                    \
+    } else if (last_t >= 0) {                                                                           \
+      pt = last_t, pk = (last_t ? cnt1 : cnt0) - 1;                                                     \
+    }                                                                                                   \
+    if (pt >= 0) {                                                                                      \
+      if (!(ok = wait_all(W, bar_s_free + 8 * pt, uint32_t(pk) & 1u))) break;                           \
+      tc_fence_after();                                                                                 \
+    }                                                                                                   \
     const uint32_t b0 = dqk_lo + ((L::KV_OFF + (ks) * L::TILE_BYTES) >> 4);                             \
     _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                             \
       const uint32_t off = (((kk / 4) * BOX_BYTES + (kk % 4) * 32) >> 4);                               \
       mma_ss_elect(d_s, a_q + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);                \
     }                                                                                                   \
-    mma_commit_elect(my_s_full);                                                                        \
+    mma_commit_elect(bar_s_full + 8 * i);                                                               \
     if ((x) + 1 == n) mma_commit_elect(bar_q_empty + 8 * qb);                                           \
   }
-        // O_i (+)= P_i V over keys in steps of 16 (stage vs of the ring)
+        // O_i (+)= P_i [V | 1] over keys in steps of 16 (stage vs of the ring)
 #define FA_ISSUE_PV(vs, acc)                                                                            \
   {                                                                                                     \
-    const uint32_t s16 = ((vs) * L::TILE_BYTES) >> 4;                                                   \
-    const uint32_t b0 = dv_lo + (L::KV_OFF >> 4) + s16;                                                 \
+    const uint32_t v_addr = sbase + L::KV_OFF + (vs) * L::TILE_BYTES;                                    \
+    const uint32_t b0 = ((v_addr >> 4) & 0x3FFFu) | (((ones_addr - v_addr) >> 4) << 16);                \
     _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                              \
       mma_ts_elect(d_o, a_p + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi, IDESC_PV, ((acc) || kk > 0) ? 1u : 0u); \
   }
@@ -444,28 +488,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tc_fence_after();                                           \
   }
         {
-          // S runs one K/V step ahead of the softmax: S_i(x) is issued once the softmax
-          // has read S_i(x-1) (s_free); P_i(j) V_j once P_i(j) is written (p_full), with
-          // a commit to o_full that the softmax waits on before it overwrites P_i or
-          // rescales O_i, and at the end of the unit.  Ring order: K_0 K_1 V_0 K_2 V_1 ...
+          // S runs one K/V step ahead of the softmax; P_i(j) V_j once P_i(j) is written (p_full),
+          // with a commit to o_full that the softmax waits on before it overwrites P_i or rescales
+          // O_i, and at the end of the unit.  Ring order: K_0 K_1 V_0 K_2 V_1 ...
           do {
             int ks = 0;
             FA_TAKE(ks);
-            if (n > 0) {
-              uint32_t par = sfr ^ 1;
-              FA_WAIT(my_s_free, par);
-              sfr ^= 1;
-              FA_ISSUE_S(ks, 0);
-            }
+            if (n > 0) FA_ISSUE_S(ks, 0);
             mma_commit_elect(bar_kv_empty + 8 * ks);
             if (nmax > 1) {
               FA_TAKE(ks);
-              if (n > 1) {
-                uint32_t par = sfr ^ 1;
-                FA_WAIT(my_s_free, par);
-                sfr ^= 1;
-                FA_ISSUE_S(ks, 1);
-              }
+              if (n > 1) FA_ISSUE_S(ks, 1);
               mma_commit_elect(bar_kv_empty + 8 * ks);
             }
           } while (0);
@@ -487,18 +520,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (j + 2 < nmax) {
               int ks = 0;
               FA_TAKE(ks);
-              if (j + 2 < n) {
-                uint32_t par = sfr ^ 1;
-                FA_WAIT(my_s_free, par);
-                sfr ^= 1;
-                FA_ISSUE_S(ks, j + 2);
-              }
+              if (j + 2 < n) FA_ISSUE_S(ks, j + 2);
               mma_commit_elect(bar_kv_empty + 8 * ks);
             }
           }
         }
         if (!ok) break;
         if (n == 0) mma_commit_elect(bar_q_empty + 8 * qb);  // this tile had nothing to do in the unit
+        cnt0 += u.n0;
+        cnt1 += u.n1;
+        last_t = u.n1 >= u.n0 ? 1 : 0;
 #undef FA_ISSUE_S
 #undef FA_ISSUE_PV
 #undef FA_TAKE
@@ -744,7 +775,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               continue;
             }
             pk[16 * c + e] = pack_bf16x2(p0, p1);
-            add_bf16x2_f32(pk[16 * c + e], lr0, lr1);  // sum of the bf16 weights
+            if (!L::ONES) add_bf16x2_f32(pk[16 * c + e], lr0, lr1);  // sum of the bf16 weights
           }
           if (F8) {
             float h0, h1;
@@ -766,7 +797,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           for (int c = 0; c < 4; ++c) tmem_st16(t_p + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
         }
         l += (la0 + la1) + (lb0 + lb1);
-        lr += lr0 + lr1;
+        if (!L::ONES) lr += lr0 + lr1;
         if (rescale) {  // o *= r; PV_i(j-1) has completed (it was issued before S_i(j), or waited for above)
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -775,6 +806,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = f2u(u2f(ov[e]) * r);
             tmem_st32(t_o + c * 32, ov);
+          }
+          if (L::ONES) {  // the weight sum the tensor core keeps beside O
+            uint32_t sv[16];
+            tmem_ld16_wait(t_o + D, sv);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[e] = f2u(u2f(sv[e]) * r);
+            tmem_st16(t_o + D, sv);
           }
         }
         tmem_wait_st();
@@ -787,6 +825,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (!(ok = W.wait(my_o_full, of_phase))) break;
       of_phase ^= 1;
       tc_fence_after();
+      if (L::ONES) lr = u2f(tmem_ld1_wait(t_o + D));  // sum of the rounded weights, from the P [V | 1] product
       const float inv_l = p.v_descale / lr;  // v_descale: 1, or the e4m3 V's scale
       if (PARTIAL) {  // this split's normalised output (fp32) and its LSE
         const int s = u.jb / p.split_tiles;
@@ -1073,21 +1112,62 @@ cudaError_t launch_split_combine(int d, const Params& p, int num_sms, cudaStream
 // allocates for that entry point.  Every device that loads the library holds
 // one copy of it until the process exits.  In host code `g_noalloc_scratch`
 // names a host-side stand-in, not device memory: its device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
+// cudaGetSymbolAddress, looked up with the device current.  The address belongs
+// to a CUDA context (a cudaDeviceReset ends the primary context; a driver-API
+// caller may make another context current), so the cache is keyed on the
+// context's process-unique id and the address is looked up again in a context
+// not seen before.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-cudaError_t noalloc_scratch_address(int dev, void** out) {
-  static void* addr[64] = {};
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+}  // namespace
+
+cudaError_t noalloc_scratch_address(void** out) {
+  struct Entry {
+    unsigned long long ctx_id;
+    void* addr;
+  };
+  static Entry cache[64] = {};
+  static int used = 0, next = 0;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
   static std::mutex mu;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // the current device is `dev`
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
+  if (!get_current || !get_id) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return cudaErrorNotSupported;
+    get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return cudaErrorNotSupported;
+    get_id = reinterpret_cast<CtxGetIdFn>(f);
   }
-  *out = addr[dev];
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) {
+    // no context current yet: the symbol lookup below makes the device's primary context current
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  }
+  for (int i = 0; i < used; ++i)
+    if (cache[i].ctx_id == id) {
+      *out = cache[i].addr;
+      return cudaSuccess;
+    }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // in the current context
+  if (e != cudaSuccess) return e;
+  Entry& slot = used < 64 ? cache[used++] : cache[next++ % 64];
+  slot.ctx_id = id;
+  slot.addr = p;
+  *out = p;
   return cudaSuccess;
 }
 
