@@ -34,12 +34,13 @@ import numpy as np  # noqa: E402
 
 import fa_inputs as fi  # noqa: E402
 
-DEFAULT_WORKLOAD = "gpt2s_causal_b8h12t1024d64"
+DEFAULT_WORKLOAD = "long_causal_b1h32t32768d128"
 METRIC = "attention fwd TFLOPS (bf16, 1 GB300) and % of dense BF16 tensor peak"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-SWEEP_DEFAULT = ["tiny_causal_b1h4t256d64", "gpt2m_b16h16t1024d64", "gpt2m_stress_b16h16t1024d64",
-                 "llama8b_causal_b1h32t4096d128", "llama8b_b1h32t4096d128", "long_causal_b1h32t32768d128"]
+SWEEP_DEFAULT = ["tiny_causal_b1h4t256d64", "gpt2s_causal_b8h12t1024d64", "gpt2m_b16h16t1024d64",
+                 "gpt2m_stress_b16h16t1024d64", "llama8b_causal_b1h32t4096d128", "llama8b_b1h32t4096d128",
+                 "long_causal_b1h32t32768d128"]
 # split-KV (fa_fwd_splitkv) entries of the sweep: workload -> key splits
 SPLITKV_SWEEP = {"tiny_causal_b1h4t256d64": 2, "gpt2s_causal_b8h12t1024d64": 2, "llama8b_b1h32t4096d128": 2}
 # grouped K/V heads: Llama-3.1-8B attention (32 query heads sharing 8 K/V heads), causal and not
@@ -74,10 +75,15 @@ def library_fingerprint():
 
 
 def recorded_traffic(workload, fingerprint):
-    """DRAM bytes per launch from an ncu summary under profiles/, if taken on this kernel build."""
+    """DRAM bytes per launch from an ncu summary under profiles/, if taken on this kernel build.
+
+    Returns (bytes, file name) or (None, None).  The figure is dram__bytes_read.sum +
+    dram__bytes_write.sum of one launch in a separate ncu capture of the same library build
+    (the summary names the command); a bench run under ncu would not give a bench value.
+    """
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
-        return None
+        return None, None
     pat = re.compile(rf"^traffic_bytes_per_launch\s+{re.escape(workload)}\s+(\d+)\s+fingerprint\s+(\w+)", re.M)
     for name in sorted(os.listdir(pdir)):
         if not name.endswith(".md"):
@@ -85,8 +91,25 @@ def recorded_traffic(workload, fingerprint):
         with open(os.path.join(pdir, name)) as f:
             for m in pat.finditer(f.read()):
                 if m.group(2) == fingerprint:
-                    return int(m.group(1))
-    return None
+                    return int(m.group(1)), name
+    return None, None
+
+
+def input_sets(w):
+    """Copies of the inputs the timed steps rotate over, so that their total exceeds 2 x L2."""
+    set_bytes = floor_bytes(w["B"], w["H"], w["T"], w["d"])
+    return max(1, math.ceil(2 * L2_BYTES / set_bytes)) if set_bytes < 2 * L2_BYTES else 1
+
+
+def workload_config(name, w, world):
+    """The `config` object both arms print for a workload."""
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    nsets = input_sets(w)
+    return {"workload": name, "B": B, "H": H, "T": T, "d": d, "causal": bool(causal),
+            "scale": 1.0 / math.sqrt(d), "qkv_dist": f"Q,K~N(0,{w['sigma_qk']}^2), V~N(0,1), bf16, seed 0",
+            "l2": f"inputs rotate over {nsets} copies ({nsets * floor_bytes(B, H, T, d) / 1e6:.0f} MB > 2x L2)"
+                  if nsets > 1 else f"one input set of {floor_bytes(B, H, T, d) / 1e6:.0f} MB, larger than 2x L2",
+            "parallelism": f"replicas x{world}", "flops_per_step": metric_flops(B, H, T, d, causal)}
 
 
 class ClockSampler:
@@ -176,8 +199,7 @@ def time_kernel(fa, torch, dev, w, qkv, steps, warmup, scale, per_step_events=Tr
     """Device-timed steps over rotating input copies; returns (total_s, per-launch mean s, nsets)."""
     B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
     q0, k0, v0 = device_inputs(qkv, torch, dev)
-    set_bytes = 4 * q0.numel() * 2 + B * H * T * 4
-    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes)) if set_bytes < 2 * L2_BYTES else 1
+    nsets = input_sets(w)
     sets = []
     for s in range(nsets):
         q, k, v = (q0, k0, v0) if s == 0 else (q0.clone(), k0.clone(), v0.clone())
@@ -209,6 +231,8 @@ def run_ours(args, world, rank, local, pg):
     peaks, peak_src = load_peaks()
     qkv = fi.make_qkv(B, H, T, d, seed=0, sigma_qk=w["sigma_qk"])
     K, W = args.steps, args.warmup
+    if K is None:  # about a quarter of a second of timed work
+        K = int(min(20000, max(20, 0.25 / max(metric_flops(B, H, T, d, causal) / 1.5e15, 1e-7))))
     # The timed region is K back-to-back calls bracketed by two events: kernels launched with
     # programmatic stream serialization overlap their set-up with the previous call's tail, which
     # an event recorded between calls would prevent.  The isolated launch time (events around each
@@ -255,9 +279,13 @@ def run_ours(args, world, rank, local, pg):
     value = world * K * f_step / total_s / 1e12
     achieved = f_step / launch_s / 1e12
     fp = library_fingerprint()
+    traffic, traffic_file = recorded_traffic(name, fp)
     roofline = {
         "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-        "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": recorded_traffic(name, fp),
+        "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
+        "traffic_source": (f"ncu capture of one launch of this library build (dram__bytes_read.sum + "
+                           f"dram__bytes_write.sum), profiles/{traffic_file}") if traffic else
+                          "no ncu capture of this library build on record",
         "peak_source": f"{peak_src} bf16 burst", "kernel": "fa_fwd_kernel",
         "floor_bytes": floor_bytes(B, H, T, d),
         "attainable_tflops": round(min(peaks["bf16_tflops"],
@@ -266,6 +294,11 @@ def run_ours(args, world, rank, local, pg):
         "achieved_isolated_launch": round(f_step / launch_iso_s / 1e12, 2),
         "launch_us_isolated": round(launch_iso_s * 1e6, 2),
     }
+    parity = None
+    if rank == 0 and not args.no_parity:
+        q, k, v, o, lse = sets[0]  # set 0 holds the seed-0 inputs themselves (the others are copies)
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
+        parity = parity_sample(qkv, o, lse, w, scale, torch)
     # the exponential unit's ceiling: one ex2 per unmasked score against 4 d tensor FLOPs
     ex2_rate = fa.fa_ex2_rate(stream)
     roofline["ex2_per_s"] = float(f"{ex2_rate:.4g}")
@@ -286,19 +319,61 @@ def run_ours(args, world, rank, local, pg):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(total_s / K * 1e3, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": name, "B": B, "H": H, "T": T, "d": d, "causal": bool(causal),
-                   "scale": scale, "qkv_dist": f"Q,K~N(0,{w['sigma_qk']}^2), V~N(0,1), bf16, seed 0",
-                   "l2": f"inputs rotate over {nsets} copies ({nsets * 4 * B * H * T * d * 2 / 1e6:.0f} MB > 2x L2)"
-                         if nsets > 1 else "one input set larger than 2x L2",
-                   "parallelism": f"replicas x{world}", "flops_per_step": f_step},
+        "config": workload_config(name, w, world),
         "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
         "roofline": roofline, "e2e": e2e, "gpu_launches": K, "clocks": clk, "cpu_baseline": cpu,
-        "library_fingerprint": fp,
+        "parity": parity, "library_fingerprint": fp,
     }
     if sweep is not None:
         line["sweep"] = sweep
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def parity_sample(qkv, o, lse, w, scale, torch, per_head=64, seed=7):
+    """O and LSE of one launch against the float64 oracle on sampled query rows of every head.
+
+    Rows per head: the first and last 16 and 32 seeded-random ones (all rows when T <= 64).
+    Tolerances: max |dO| <= 1e-2 (plus half a bf16 spacing where |O_ref| >= 4, where
+    correct rounding alone can exceed 1e-2), mean |dO| <= 1e-3, max |dLSE| <= 1e-3.
+    """
+    import oracle
+
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    torch.cuda.synchronize()
+    o_bits = o.view(torch.int16).cpu().numpy().view(np.uint16)
+    lse_h = lse.cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(seed)
+    t0 = time.perf_counter()
+    q, k, v = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    o_err_max = o_err_sum = lse_err_max = 0.0
+    n = wide = 0
+    ok = True
+    for b in range(B):
+        for h in range(H):
+            if T <= per_head:
+                rows = np.arange(T)
+            else:
+                rows = np.unique(np.concatenate([np.arange(16), np.arange(T - 16, T),
+                                                 rng.integers(0, T, size=per_head - 32)]))
+            o_ref, l_ref = oracle.attention_head(q[b, h], k[b, h], v[b, h], causal, scale, rows=rows)
+            o_gpu = fi.bf16_bits_to_f64(o_bits[b, h, rows])
+            err = np.abs(o_gpu - o_ref)
+            half_ulp = np.ldexp(1.0, np.frexp(np.where(np.abs(o_ref) > 0, np.abs(o_ref), 1.0))[1] - 9)
+            tol = np.where(np.abs(o_ref) >= 4.0, 1e-2 + half_ulp, 1e-2)
+            ok &= bool((err <= tol).all())
+            wide += int((err > 1e-2).sum())
+            o_err_max = max(o_err_max, float(err.max()))
+            o_err_sum += float(err.sum())
+            n += err.size
+            lse_err_max = max(lse_err_max, float(np.abs(lse_h[b, h, rows] - l_ref).max()))
+    mean = o_err_sum / n
+    ok = ok and mean <= 1e-3 and lse_err_max <= 1e-3
+    return {"o_max_abs": float(f"{o_err_max:.4g}"), "o_mean_abs": float(f"{mean:.4g}"),
+            "lse_max_abs": float(f"{lse_err_max:.4g}"), "o_beyond_1e-2_where_abs_o_ge_4": wide,
+            "pass": bool(ok), "rows_checked": n // d, "oracle_s": round(time.perf_counter() - t0, 1),
+            "against": f"float64 oracle on {per_head} sampled query rows per head (first 16, last 16, "
+                       f"seeded random), seed-0 inputs"}
 
 
 def run_e2e(fa, torch, dev, w, qkv, scale, steps, pg):
@@ -556,21 +631,28 @@ def oracle_threads():
     return os.cpu_count() or 1
 
 
+def spread_rows(T, count, offset):
+    """`count` query rows spread evenly over [0, T), shifted by `offset`: a causal row's cost grows
+    with its index, so evenly spread rows cost what the average row of the workload costs."""
+    count = max(1, min(T, count))
+    stride = T / count
+    return np.unique((offset % max(1, int(stride)) + np.floor(np.arange(count) * stride)).astype(np.int64) % T)
+
+
 def cpu_baseline(w, qkv, scale, seconds):
     """The float64 oracle, as it stands, on heads of the same input until ~`seconds` of CPU work."""
     import oracle
 
     B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
     q, k, v = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
-    rows_per_block = T if T <= 4096 else 256
+    rows_per_block = min(T, 256)
     heads = [(b, h) for b in range(B) for h in range(H)]
     done_rows = 0
     t0 = time.perf_counter()
     it = 0
     while True:
         b, h = heads[it % len(heads)]
-        r0 = (it // len(heads)) * rows_per_block % T
-        rows = np.arange(r0, min(T, r0 + rows_per_block))
+        rows = spread_rows(T, rows_per_block, it // len(heads))
         oracle.attention_head(q[b, h], k[b, h], v[b, h], causal, scale, rows=rows)
         done_rows += len(rows)
         it += 1
@@ -579,8 +661,9 @@ def cpu_baseline(w, qkv, scale, seconds):
     dt = time.perf_counter() - t0
     f = metric_flops(1, 1, T, d, causal) / T * done_rows  # metric FLOPs of the rows evaluated
     return {"value": round(f / dt / 1e12, 6), "unit": "TFLOPS", "cores": oracle_threads(), "kind": "oracle",
-            "sample": f"{done_rows} query rows ({done_rows / (B * H * T):.3f} of the workload) in "
-                      f"{rows_per_block}-row blocks, {dt:.1f} s, float64 numpy"}
+            "sample": f"{done_rows} query rows ({done_rows / (B * H * T):.4f} of the workload) in blocks of "
+                      f"{rows_per_block} rows spread evenly over T, {dt:.1f} s, float64 numpy; the metric's FLOPs "
+                      f"of those rows over the time"}
 
 
 def run_reference(args, world, rank):
@@ -595,18 +678,19 @@ def run_reference(args, world, rank):
     scale = 1.0 / math.sqrt(d)
     qkv = fi.make_qkv(B, H, T, d, seed=0, sigma_qk=w["sigma_qk"])
     q, k, v = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
-    K, W = args.steps, args.warmup
+    K = args.steps if args.steps is not None else 20
+    W = args.warmup
     # rows per step so that the whole run stays within about `budget` seconds
     t0 = time.perf_counter()
-    oracle.attention_head(q[0, 0], k[0, 0], v[0, 0], causal, scale, rows=np.arange(min(T, 64)))
-    per_row = (time.perf_counter() - t0) / min(T, 64)
+    probe = spread_rows(T, 64, 0)
+    oracle.attention_head(q[0, 0], k[0, 0], v[0, 0], causal, scale, rows=probe)
+    per_row = (time.perf_counter() - t0) / len(probe)
     rows = int(max(1, min(T, args.reference_budget / max(K + W, 1) / max(per_row, 1e-9))))
     heads = [(b, h) for b in range(B) for h in range(H)]
 
     def step(i):
         b, h = heads[i % len(heads)]
-        r0 = (i // len(heads)) * rows % T
-        rr = np.arange(r0, min(T, r0 + rows))
+        rr = spread_rows(T, rows, i // len(heads))
         oracle.attention_head(q[b, h], k[b, h], v[b, h], causal, scale, rows=rr)
         return len(rr)
 
@@ -617,12 +701,13 @@ def run_reference(args, world, rank):
     dt = time.perf_counter() - t0
     f = metric_flops(1, 1, T, d, causal) / T * n_rows
     value = f / dt / 1e12
-    sample = f"{rows} query rows of one head per step ({n_rows} rows in {K} steps), float64 numpy"
+    sample = (f"{rows} query rows of one head per step, spread evenly over T ({n_rows} rows in {K} steps), "
+              f"float64 numpy; the metric's FLOPs of those rows over the time")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(dt / K * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, "B": B, "H": H, "T": T, "d": d, "causal": bool(causal), "scale": scale},
+        "config": workload_config(name, w, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": oracle_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -633,7 +718,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 0.25 s of work)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fi.WORKLOADS))
@@ -642,6 +727,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--sweep", default=",".join(SWEEP_DEFAULT))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-budget", type=float, default=90.0)
     args = ap.parse_args()
