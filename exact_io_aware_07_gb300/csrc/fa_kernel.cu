@@ -15,32 +15,34 @@
 // otherwise the stale m is kept, so p <= 2^8, and the final o / l and the LSE
 // use that same m, which keeps the result exact up to rounding.
 //
-// Two row sums are kept: lr sums the bf16-rounded weights p~ that the P V MMA
+// Two row sums are kept: lr sums the rounded weights p~ that the P V MMA
 // multiplies by, and O = sum p~ v / lr is a convex combination of the value
 // rows under exactly the weights used (a row dominated by one key returns that
 // key's value row unchanged, whatever the stale m); l sums the fp32 weights and
-// gives the LSE without the bf16 rounding of the weights.
+// gives the LSE without the rounding of the weights.  At d = 64 and for e4m3
+// the tensor core forms lr itself: as 16 extra columns of O_i += P_i [V_j | 1]
+// (d = 64), or as L_i += P_i x ones, a product of its own (e4m3).
 //
 // Roles (one CTA per SM, persistent over work units):
 //   warps 0-3  softmax for query tile 0 of the unit (one TMEM lane = one row per thread)
-//   warps 4-7  softmax for query tile 1 (d = 64: the tiles of a causal unit may be handed
-//              to the two slots the other way round, see balance_slots)
+//   warps 4-7  softmax for query tile 1 (d = 64, e4m3: the tiles of a causal unit may be
+//              handed to the two slots the other way round, see balance_slots)
 //   warp 8     TMA producer: Q tiles once per unit, then K_j, V_j through a ring
-//   warp 9     Tensor Memory allocator; tcgen05.mma issuer (d = 128: both tiles;
-//              d = 64: tile 0)
-//   warp 10    d = 64 only: tcgen05.mma issuer for tile 1 (warp 11 only joins the
-//              final barrier; 384 threads at d = 64, 320 at d = 128)
+//   warp 9     Tensor Memory allocator; tcgen05.mma issuer (bf16 d = 128: both tiles;
+//              d = 64 and e4m3: tile 0)
+//   warp 10    d = 64 and e4m3: tcgen05.mma issuer for tile 1 (warp 11 only joins the
+//              final barrier; 384 threads there, 320 at bf16 d = 128)
 // The issuing warps run their schedules on all 32 lanes (every operand stays
 // warp-uniform); elect.sync inside each TMA, MMA and commit picks the lane that
 // issues it.
 // A work unit is (batch*head, 256 query rows) = two 128-row query tiles that
-// share every K/V tile loaded.  Tensor Memory (512 columns, fp32):
-//   S_0 [0,128)  S_1 [128,256)  O_0 [256,256+d)  O_1 [256+d,256+2d)
-// d = 128: P_i (bf16 pairs) is written over the first 64 columns of S_i once S_i
-// has been read, so S_i(j+1) waits for P_i(j) V_j.  d = 64: P_0 [384,448) and
-// P_1 [448,512) have columns of their own, so S_i(j+1) is computed while the
-// softmax of S_i(j) runs, and each tile's MMAs are issued by a warp of its own
-// that waits only on that tile's barriers.
+// share every K/V tile loaded.  Tensor Memory (512 columns, fp32), bf16 d = 128:
+//   S_0 [0,128)  S_1 [128,256)  O_0 [256,384)  O_1 [384,512)
+// with P_i (bf16 pairs) written over the first 64 columns of S_i once S_i has
+// been read, so S_i(j+1) waits for P_i(j) V_j.  d = 64 and e4m3: one S buffer
+// [0,128) that the two tiles' products take in turn, then O_0, O_1 and P_0, P_1
+// in columns of their own, so the next S is computed while the softmax of S_i(j)
+// runs, and each tile's MMAs are issued by a warp of its own.
 // O leaves through shared memory: each softmax warp writes its 32 rows x 64
 // columns in the 128-byte swizzled layout of the output tensor map and one lane
 // stores them with a TMA tensor store, so every store moves whole rows.
@@ -76,18 +78,23 @@ struct Layout {
   // d = 64 and e4m3: two units' Q tiles resident (the next unit's load overlaps the
   // current unit); bf16 d = 128: one unit's Q tiles, the next unit's prefetched into L2.
   static constexpr int QBUF = (D == 128 && !F8) ? 1 : 2;
-  static constexpr int STAGES = (D == 128 && !F8) ? 4 : 6;     // K/V ring depth (tiles)
+  static constexpr int STAGES = (D == 128 && !F8) ? 4 : (F8 ? 5 : 6);  // K/V ring depth (tiles)
   static constexpr int Q_OFF = 0;                      // [QBUF units][2 query tiles]
   static constexpr int KV_OFF = QBUF * 2 * TILE_BYTES;
-  // d = 64: P_i has Tensor Memory columns of its own, so the next S may be computed
-  // while the softmax of S_i(j) runs (see the MMA issuer); d = 128: P_i overwrites S_i.
-  static constexpr bool SEP_P = (D == 64) && !F8;
+  // d = 64 and e4m3: P_i has Tensor Memory columns of its own and the two query tiles' S
+  // products share one buffer, so the next S may be computed while the softmax of S_i(j) runs
+  // (see the MMA issuers); bf16 d = 128: P_i overwrites S_i, each tile has its own S buffer.
+  static constexpr bool SEP_P = D == 64 || F8;
   // d = 64: O_i += P_i [V_j | 1]: the P V product also forms the sum of the rounded weights
   // (16 columns of ones after V, read from a constant block in shared memory), which divides O.
-  static constexpr bool ONES = SEP_P;
+  static constexpr bool ONES = SEP_P && D == 64 && !F8;
   static constexpr int ON = D;                          // O columns per query tile in TMEM
   static constexpr int ON_MMA = ONES ? D + 16 : D;      // columns the P V product writes
-  // d = 64: one MMA-issuing warp per query tile (warps 9, 10; warp 11 idle); d = 128: warp 9 alone
+  // e4m3: L_i += P_i x ones (16 columns of one), a product of its own that forms the sum of the
+  // rounded weights; its B operand is a constant K-major block of e4m3 ones (16 rows x 128 keys)
+  static constexpr bool LSUM = F8;
+  // d = 64 and e4m3: one MMA-issuing warp per query tile (warps 9, 10; warp 11 idle);
+  // bf16 d = 128: warp 9 alone
   static constexpr int THREADS = SEP_P ? 384 : 320;
   static constexpr int MMA_WARPS = SEP_P ? 2 : 1;
   // bf16 O staging per softmax warp: 32 rows x 64 columns (4 KB, 128-byte swizzle), and for
@@ -98,27 +105,33 @@ struct Layout {
   static constexpr int STG_WARP_BYTES = (STG2 ? 2 : 1) * 32 * 128;
   // d = 64: the ones block, laid out as one more 64-column V atom (128 rows of 128 bytes, 1 KB aligned)
   static constexpr int ONES_OFF = STG_OFF + 8 * STG_WARP_BYTES;
-  static constexpr int ONES_BYTES = ONES ? 128 * 128 : 0;
+  static constexpr int ONES_BYTES = ONES ? 128 * 128 : (LSUM ? 16 * 128 : 0);
   static constexpr int BAR_OFF = ONES_OFF + ONES_BYTES;
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2],
   // s_free[2], done
   static constexpr int NUM_BARS = 4 + 2 * STAGES + 10 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // TMEM base slot, abort flag
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
-  // Tensor Memory columns.  d = 128 and e4m3: S_0 [0,128), S_1 [128,256), O_0, O_1 after them, P_i
+  // Tensor Memory columns.  bf16 d = 128: S_0 [0,128), S_1 [128,256), O_0, O_1 after them, P_i
   // over S_i.  d = 64: one S buffer [0,128) that the two query tiles' products take in turn,
   // O_0 [128,208) and O_1 [224,304) (64 columns of O and 16 of the weight sum each),
-  // P_0 [320,384) and P_1 [384,448).
+  // P_0 [320,384) and P_1 [384,448).  e4m3: S [0,128), O_0 [128,256), O_1 [256,384),
+  // P_0 [384,416), P_1 [416,448) (four e4m3 weights per column), L_0 [448,464), L_1 [464,480).
+  static constexpr uint32_t OSTRIDE = ONES ? 96u : uint32_t(D);  // Tensor Memory columns per O_i
+  static constexpr uint32_t PCOLS = F8 ? 32u : 64u;                // columns of P_i (4 e4m3 or 2 bf16 each)
   static __device__ __forceinline__ constexpr uint32_t s_col(int i) { return SEP_P ? 0u : uint32_t(i) * 128u; }
   static __device__ __forceinline__ constexpr uint32_t o_col(int i) {
-    return SEP_P ? 128u + uint32_t(i) * 96u : 256u + uint32_t(i) * ON;
+    return SEP_P ? 128u + uint32_t(i) * OSTRIDE : 256u + uint32_t(i) * ON;
   }
   static __device__ __forceinline__ constexpr uint32_t p_col(int i) {
-    return SEP_P ? 320u + uint32_t(i) * 64u : s_col(i);
+    return SEP_P ? 128u + 2u * OSTRIDE + uint32_t(i) * PCOLS : s_col(i);
   }
+  static __device__ __forceinline__ constexpr uint32_t l_col(int i) { return 448u + uint32_t(i) * 16u; }
 };
-static_assert(Layout<64>::ON_MMA <= 96 && 320 + 2 * 64 <= 512, "Tensor Memory columns exceed 512");
-static_assert(Layout<64>::ONES_OFF % 1024 == 0, "the ones block must be 1 KB aligned like the V tiles");
+static_assert(Layout<64>::p_col(1) + 64 <= 512 && Layout<128>::p_col(1) + 64 <= 512 &&
+              Layout<128, true>::p_col(1) + 32 <= 512, "Tensor Memory columns exceed 512");
+static_assert(Layout<64>::ONES_OFF % 1024 == 0 && Layout<128, true>::ONES_OFF % 1024 == 0,
+              "the ones block must be 1 KB aligned like the tiles");
 
 constexpr int MAX_SMEM_PER_CTA = 232448;  // 227 KB opt-in dynamic shared memory per block on sm_103
 static_assert(Layout<64>::SMEM_BYTES <= MAX_SMEM_PER_CTA && Layout<128>::SMEM_BYTES <= MAX_SMEM_PER_CTA,
@@ -247,9 +260,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
-  if (L::ONES) {  // bf16 1.0 everywhere in the block; the tensor core reads it through the async proxy
+  if (L::ONES || L::LSUM) {  // 1.0 everywhere in the block; the tensor core reads it through the async proxy
+    const uint32_t one = L::LSUM ? 0x38383838u : 0x3F803F80u;  // e4m3 or bf16 ones
     for (int t = threadIdx.x; t < L::ONES_BYTES / 16; t += L::THREADS)
-      st_shared_v4(sbase + L::ONES_OFF + 16 * t, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+      st_shared_v4(sbase + L::ONES_OFF + 16 * t, one, one, one, one);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -405,19 +419,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // are strictly ordered, the awaited completion is always the next one of that barrier.
     {
       const int i = warp - MMA_WARP0;  // query tile of this warp
-      constexpr uint32_t IDESC_S = make_idesc_bf16(BM, BN, 0);          // S = Q K^T: both K-major
-      constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, L::ON_MMA, 1);  // O += P [V | 1]: V is MN-major
+      constexpr uint32_t IDESC_S = F8 ? make_idesc_e4m3(BM, BN) : make_idesc_bf16(BM, BN, 0);  // both K-major
+      // O += P [V | 1] (d = 64), O += P V (V MN-major), or e4m3 O += P (V^T)^T (both K-major)
+      constexpr uint32_t IDESC_PV = F8 ? make_idesc_e4m3(BM, L::ON) : make_idesc_bf16(BM, L::ON_MMA, 1);
+      constexpr int KSTEP = F8 ? 32 : 16;  // reduction depth of one MMA
       // Descriptor halves: the address field (low 14 bits, in 16-byte units) and, for V, the
       // leading byte offset (bits 16-29: from the V tile to the ones block, the second 64-column
       // atom of B) are the parts that change; every offset added below stays inside its field.
       const uint64_t dqk = make_sdesc_sw128(sbase, 16, 1024);        // K-major tiles (Q, K)
       const uint64_t dvv = make_sdesc_sw128(sbase, BOX_BYTES, 1024);  // MN-major V tiles
       const uint32_t dqk_lo = uint32_t(dqk), dqk_hi = uint32_t(dqk >> 32);
-      const uint32_t dv_hi = uint32_t(dvv >> 32);
+      const uint32_t dv_lo = uint32_t(dvv), dv_hi = uint32_t(dvv >> 32);
       const uint32_t ones_addr = sbase + L::ONES_OFF;
       const uint32_t my_p_full = bar_p_full + 8 * i;
       const uint32_t my_o_full = bar_o_full + 8 * i, my_o_empty = bar_o_empty + 8 * i;
       const uint32_t d_s = tmem + L::s_col(i), d_o = tmem + L::o_col(i), a_p = tmem + L::p_col(i);
+      const uint32_t d_l = tmem + L::l_col(i);
+      constexpr uint32_t IDESC_L = make_idesc_e4m3(BM, 16);
+      const uint32_t ones_lo = uint32_t(make_sdesc_sw128(ones_addr, 16, 1024));
       int stage = 0;
       uint32_t phase = 0;
       uint32_t pf = 0, oe = 0;
@@ -456,9 +475,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tc_fence_after();                                                                                 \
     }                                                                                                   \
     const uint32_t b0 = dqk_lo + ((L::KV_OFF + (ks) * L::TILE_BYTES) >> 4);                             \
-    _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                             \
+    _Pragma("unroll") for (int kk = 0; kk < D / KSTEP; ++kk) {                                          \
       const uint32_t off = (((kk / 4) * BOX_BYTES + (kk % 4) * 32) >> 4);                               \
-      mma_ss_elect(d_s, a_q + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);                \
+      if (F8)                                                                                           \
+        mma_f8_ss_elect(d_s, a_q + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);           \
+      else                                                                                              \
+        mma_ss_elect(d_s, a_q + off, dqk_hi, b0 + off, dqk_hi, IDESC_S, kk > 0 ? 1u : 0u);              \
     }                                                                                                   \
     mma_commit_elect(bar_s_full + 8 * i);                                                               \
     if ((x) + 1 == n) mma_commit_elect(bar_q_empty + 8 * qb);                                           \
@@ -467,9 +489,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #define FA_ISSUE_PV(vs, acc)                                                                            \
   {                                                                                                     \
     const uint32_t v_addr = sbase + L::KV_OFF + (vs) * L::TILE_BYTES;                                    \
-    const uint32_t b0 = ((v_addr >> 4) & 0x3FFFu) | (((ones_addr - v_addr) >> 4) << 16);                \
-    _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                              \
-      mma_ts_elect(d_o, a_p + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi, IDESC_PV, ((acc) || kk > 0) ? 1u : 0u); \
+    if (F8) {                                                                                           \
+      const uint32_t b0 = dqk_lo + ((L::KV_OFF + (vs) * L::TILE_BYTES) >> 4);                           \
+      _Pragma("unroll") for (int kk = 0; kk < BN / KSTEP; ++kk)                                         \
+        mma_f8_ts_elect(d_o, a_p + kk * 8, b0 + ((kk * 32) >> 4), dqk_hi, IDESC_PV, ((acc) || kk > 0) ? 1u : 0u); \
+      if (L::LSUM)                                                                                      \
+        _Pragma("unroll") for (int kk = 0; kk < BN / KSTEP; ++kk)                                       \
+          mma_f8_ts_elect(d_l, a_p + kk * 8, ones_lo + ((kk * 32) >> 4), dqk_hi, IDESC_L,                \
+                          ((acc) || kk > 0) ? 1u : 0u);                                                 \
+    } else {                                                                                            \
+      const uint32_t b0 = L::ONES ? (((v_addr >> 4) & 0x3FFFu) | (((ones_addr - v_addr) >> 4) << 16))  \
+                                  : dv_lo + ((L::KV_OFF + (vs) * L::TILE_BYTES) >> 4);                  \
+      _Pragma("unroll") for (int kk = 0; kk < BN / 16; ++kk)                                            \
+        mma_ts_elect(d_o, a_p + kk * 8, b0 + ((kk * 2048) >> 4), dv_hi, IDESC_PV, ((acc) || kk > 0) ? 1u : 0u); \
+    }                                                                                                   \
   }
 #define FA_TAKE(slot)                                                      \
   {                                                                        \
@@ -771,18 +804,21 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 pk[8 * c + e / 2] |= b2 << 16;
               else
                 pk[8 * c + e / 2] = b2;
-              h8 = add_f16x2(h8, e4m3x2_to_f16x2(b2));
+              if (!L::LSUM) h8 = add_f16x2(h8, e4m3x2_to_f16x2(b2));
               continue;
             }
             pk[16 * c + e] = pack_bf16x2(p0, p1);
             if (!L::ONES) add_bf16x2_f32(pk[16 * c + e], lr0, lr1);  // sum of the bf16 weights
           }
           if (F8) {
-            float h0, h1;
-            f16x2_to_f32(h8, h0, h1);
-            lr0 += h0;
-            lr1 += h1;
-            if (c & 1) tmem_st16(t_p + (c / 2) * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * (c / 2)));
+            if (!L::LSUM) {
+              float h0, h1;
+              f16x2_to_f32(h8, h0, h1);
+              lr0 += h0;
+              lr1 += h1;
+            }
+            if (!L::SEP_P && (c & 1))
+              tmem_st16(t_p + (c / 2) * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * (c / 2)));
           } else if (!L::SEP_P) {
             tmem_st16(t_p + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
           }
@@ -794,10 +830,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tc_fence_after();
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_st16(t_p + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
+          for (int c = 0; c < int(L::PCOLS) / 16; ++c)
+            tmem_st16(t_p + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
         }
         l += (la0 + la1) + (lb0 + lb1);
-        if (!L::ONES) lr += lr0 + lr1;
+        if (!L::ONES && !L::LSUM) lr += lr0 + lr1;
         if (rescale) {  // o *= r; PV_i(j-1) has completed (it was issued before S_i(j), or waited for above)
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -806,6 +843,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = f2u(u2f(ov[e]) * r);
             tmem_st32(t_o + c * 32, ov);
+          }
+          if (L::LSUM) {
+            const uint32_t t_l = tmem + lane_off + L::l_col(i);
+            tmem_st1(t_l, f2u(u2f(tmem_ld1_wait(t_l)) * r));
           }
           if (L::ONES) {  // the weight sum the tensor core keeps beside O
             uint32_t sv[16];
@@ -826,6 +867,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       of_phase ^= 1;
       tc_fence_after();
       if (L::ONES) lr = u2f(tmem_ld1_wait(t_o + D));  // sum of the rounded weights, from the P [V | 1] product
+      if (L::LSUM) lr = u2f(tmem_ld1_wait(tmem + lane_off + L::l_col(i)));  // from the P x ones product
       const float inv_l = p.v_descale / lr;  // v_descale: 1, or the e4m3 V's scale
       if (PARTIAL) {  // this split's normalised output (fp32) and its LSE
         const int s = u.jb / p.split_tiles;
