@@ -41,8 +41,11 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 SWEEP_DEFAULT = ["tiny_causal_b1h4t256d64", "gpt2s_causal_b8h12t1024d64", "gpt2m_b16h16t1024d64",
                  "gpt2m_stress_b16h16t1024d64", "llama8b_causal_b1h32t4096d128", "llama8b_b1h32t4096d128",
                  "long_causal_b1h32t32768d128"]
-# split-KV (fa_fwd_splitkv) entries of the sweep: workload -> key splits
-SPLITKV_SWEEP = {"tiny_causal_b1h4t256d64": 2, "gpt2s_causal_b8h12t1024d64": 2, "llama8b_b1h32t4096d128": 2}
+# split-KV (fa_fwd_splitkv, split count chosen by the library) against fa_fwd on the same inputs: shapes
+# with fewer work units than SMs, where one head's long rows would otherwise leave SMs idle
+SPLITKV_SWEEP = {"splitkv_tiny_causal_b1h4t256d64": dict(B=1, H=4, T=256, d=64, causal=True),
+                 "splitkv_prefill_causal_b1h4t8192d128": dict(B=1, H=4, T=8192, d=128, causal=True),
+                 "splitkv_prefill_b1h2t16384d64": dict(B=1, H=2, T=16384, d=64, causal=False)}
 # grouped K/V heads: Llama-3.1-8B attention (32 query heads sharing 8 K/V heads), causal and not
 GQA_SWEEP = {"llama8b_gqa_causal_b1h32kv8t4096d128": dict(B=1, H=32, Hkv=8, T=4096, d=128, causal=True),
              "llama8b_gqa_b1h32kv8t4096d128": dict(B=1, H=32, Hkv=8, T=4096, d=128, causal=False)}
@@ -433,23 +436,33 @@ def run_e2e(fa, torch, dev, w, qkv, scale, steps, pg):
             "path": "exact_io_aware_07_gb300.attention() with pinned host buffers, steps alternating on two streams"}
 
 
-def time_splitkv(fa, torch, dev, w, qkv, scale, num_splits, steps):
-    """Device time of fa_fwd_splitkv (both kernels) per step, inputs rotating past L2."""
-    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
-    sets, stream, ev, start, end, nsets = time_kernel(fa, torch, dev, w, qkv, steps, 0, scale, True)
-    ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits), dtype=torch.uint8, device=dev)
-    for i in range(5):
-        q, k, v, o, lse = sets[i % nsets]
-        fa.fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, ws, stream)
+def time_splitkv(fa, torch, dev, g, steps):
+    """Device time per call of fa_fwd and of fa_fwd_splitkv (automatic split count), calls alternating."""
+    B, H, T, d, causal = g["B"], g["H"], g["T"], g["d"], g["causal"]
+    x = fi.make_qkv(B, H, T, d, seed=0)
+    q, k, v = device_inputs(x, torch, dev)
+    o, lse = torch.empty_like(q), torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, 0), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(d)
+    stream = torch.cuda.current_stream(dev)
+    runs = {"unsplit": lambda: fa.fa_fwd(q, k, v, o, lse, causal, scale, stream),
+            "split": lambda: fa.fa_fwd_splitkv(q, k, v, o, lse, causal, scale, 0, ws, stream)}
+    for _ in range(5):
+        for r in runs.values():
+            r()
     torch.cuda.synchronize(dev)
+    ev = {n: [] for n in runs}
     for i in range(steps):
-        q, k, v, o, lse = sets[i % nsets]
-        ev[i][0].record(stream)
-        fa.fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, ws, stream)
-        ev[i][1].record(stream)
+        for n, r in runs.items():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            r()
+            b.record(stream)
+            ev[n].append((a, b))
     torch.cuda.synchronize(dev)
-    ms = [a.elapsed_time(b) for a, b in ev]
-    return sum(ms) / len(ms) / 1e3, ws.numel()
+    if fa.fa_device_status(stream) != 0:
+        raise RuntimeError("a bounded in-kernel wait ran out in the split-KV sweep")
+    return {n: sorted(a.elapsed_time(b) for a, b in e)[len(e) // 2] / 1e3 for n, e in ev.items()}, ws.numel()
 
 
 def time_gqa(fa, torch, dev, g, steps):
@@ -583,16 +596,16 @@ def run_sweep(fa, torch, dev, names, peaks, splitkv=SPLITKV_SWEEP, gqa=GQA_SWEEP
                      "pct_of_bf16_peak": round(100 * f / sec / 1e12 / peaks["bf16_tflops"], 1),
                      "steps": steps, "kernels": "fa_fwd_kernel (grouped K/V heads)"}
         torch.cuda.empty_cache()
-    for name, ns in splitkv.items():
-        w = fi.WORKLOADS[name]
-        qkv = fi.make_qkv(w["B"], w["H"], w["T"], w["d"], seed=0, sigma_qk=w["sigma_qk"])
-        f = metric_flops(w["B"], w["H"], w["T"], w["d"], w["causal"])
-        steps = int(min(2000, max(20, 0.5 / max(f / 1.0e15, 1e-6))))
-        sec, ws_bytes = time_splitkv(fa, torch, dev, w, qkv, 1.0 / math.sqrt(w["d"]), ns, steps)
-        out[f"splitkv{ns}_{name}"] = {"ms_mean": round(sec * 1e3, 4), "tflops": round(f / sec / 1e12, 1),
-                                      "pct_of_bf16_peak": round(100 * f / sec / 1e12 / peaks["bf16_tflops"], 1),
-                                      "steps": steps, "workspace_bytes": ws_bytes,
-                                      "kernels": "fa_fwd_kernel (partial) + fa_split_combine_kernel"}
+    for name, g in splitkv.items():
+        f = metric_flops(g["B"], g["H"], g["T"], g["d"], g["causal"])
+        steps = int(min(1000, max(20, 0.3 / max(f / 1.0e15, 1e-6))))
+        sec, ws_bytes = time_splitkv(fa, torch, dev, g, steps)
+        out[name] = {"ms_median_split": round(sec["split"] * 1e3, 4), "ms_median_unsplit": round(sec["unsplit"] * 1e3, 4),
+                     "tflops_split": round(f / sec["split"] / 1e12, 1),
+                     "tflops_unsplit": round(f / sec["unsplit"] / 1e12, 1),
+                     "speedup": round(sec["unsplit"] / sec["split"], 3), "steps": steps, "workspace_bytes": ws_bytes,
+                     "num_splits": "chosen by the library (0)",
+                     "kernels": "fa_fwd_kernel (partial, last split of each 32-row group merges) vs fa_fwd_kernel"}
         torch.cuda.empty_cache()
     for name in names:
         w = fi.WORKLOADS[name]

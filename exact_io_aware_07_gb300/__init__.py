@@ -328,7 +328,7 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=
 
 
 def fa_fwd_splitkv_workspace_bytes(B: int, H: int, T: int, d: int, num_splits: int) -> int:
-    """Bytes of scratch ``fa_fwd_splitkv`` needs (0 for invalid sizes)."""
+    """Bytes of scratch ``fa_fwd_splitkv`` needs (0 for invalid sizes; ``num_splits`` 0: the automatic choice)."""
     return int(load_library().fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits))
 
 
@@ -359,8 +359,8 @@ def fa_fwd_splitkv(q, k, v, o, lse, causal: bool, scale: float, num_splits: int,
         raise FAError(code, "fa_fwd_splitkv")
 
 
-def attention_splitkv(q, k, v, causal: bool = False, num_splits: int = 2, scale: float | None = None, stream=None):
-    """Allocates O, LSE and the split workspace and runs ``fa_fwd_splitkv``."""
+def attention_splitkv(q, k, v, causal: bool = False, num_splits: int = 0, scale: float | None = None, stream=None):
+    """Allocates O, LSE and the split workspace and runs ``fa_fwd_splitkv`` (``num_splits`` 0: chosen by the library)."""
     import torch
 
     B, H, T, d = q.shape

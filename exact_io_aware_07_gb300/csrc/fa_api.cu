@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -246,7 +247,32 @@ fa_status prepare(const void* q, const void* k, const void* v, void* o, float* l
   return FA_OK;
 }
 
-// Split-KV launch: partials into `ws` ([splits][rows][d] outputs, then [splits][rows] LSE), then the merge.
+// Key splits chosen for num_splits == 0: enough that the longest unit's share of the keys fits in
+// the average work per SM (units of 256 query rows, work counted in 128-key tiles), at most 16;
+// 1 when the units alone fill the SMs evenly enough.
+int auto_splits(int B, int H, int T, int causal, int num_sms) {
+  const long long nk = (T + 127) / 128, nqb = (T + 255) / 256;
+  long long work = 0;  // K/V tiles over all units
+  for (long long qb = 0; qb < nqb; ++qb) work += causal ? std::min(nk, 2 * qb + 2) : nk;
+  work *= static_cast<long long>(B) * H;
+  const double per_sm = static_cast<double>(work) / num_sms;
+  const long long longest = causal ? std::min(nk, 2 * nqb) : nk;
+  long long s = per_sm >= 1.0 ? static_cast<long long>(std::ceil(longest / per_sm)) : longest;
+  return static_cast<int>(std::max(1LL, std::min({s, nk, 16LL})));
+}
+
+// Workspace layout of the split form: [splits][B*H*T][d] fp32 partial outputs, [splits][B*H*T]
+// fp32 partial LSE, then one int counter per 32 query rows of every head.
+size_t splitkv_bytes(int B, int H, int T, int d, int num_splits) {
+  const size_t rows = static_cast<size_t>(B) * H * T;
+  const size_t counters = static_cast<size_t>(B) * H * ((T + 31) / 32);
+  const size_t bytes = static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 1) * 4 + counters * 4;
+  return (bytes + 255) / 256 * 256;
+}
+
+// Split-KV launch: one kernel over (query block, key split) units.  The counters are cleared
+// first (an asynchronous memset on the stream; nothing is allocated); each split writes its
+// partials and the last split of every 32-row group merges the group into O and LSE.
 fa_status launch_splitkv(Prepared& pr, int d, int num_splits, float* ws, cudaStream_t stream) {
   fa::Params& p = pr.p;
   p.split_tiles = (p.nk + num_splits - 1) / num_splits;
@@ -254,12 +280,14 @@ fa_status launch_splitkv(Prepared& pr, int d, int num_splits, float* ws, cudaStr
   const size_t rows = static_cast<size_t>(p.BH) * p.T;
   p.opart = ws;
   p.lsepart = ws + static_cast<size_t>(p.num_splits) * rows * d;
+  p.counters = reinterpret_cast<int*>(p.lsepart + static_cast<size_t>(p.num_splits) * rows);
+  p.ngroups = (p.T + 31) / 32;
   const long long units = static_cast<long long>(p.BH) * p.nqb * p.num_splits;
   if (units > INT_MAX) return FA_ERR_BAD_SHAPE;
   p.num_units = static_cast<int>(units);
   const int grid = p.num_units < pr.num_sms ? p.num_units : pr.num_sms;
-  if (fa::launch_fa_fwd_partial(d, pr.tq, pr.tk, pr.tv, p, grid, stream) != cudaSuccess ||
-      fa::launch_split_combine(d, p, pr.num_sms, stream) != cudaSuccess) {
+  if (cudaMemsetAsync(p.counters, 0, static_cast<size_t>(p.BH) * p.ngroups * sizeof(int), stream) != cudaSuccess ||
+      fa::launch_fa_fwd_partial(d, pr.tq, pr.tk, pr.tv, p, grid, stream) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
@@ -357,11 +385,12 @@ fa_status fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, 
 
 fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                  int T, int d, int causal, float scale, int num_splits, cudaStream_t stream) {
-  if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_BAD_ARG;
+  if (num_splits < 0 || num_splits > FA_MAX_SPLITS) return FA_ERR_BAD_ARG;
   Prepared pr;
   fa_status st = prepare(q, k, v, o, lse, B, H, H, T, d, causal, scale, &pr);
   if (st != FA_OK) return st;
-  if (fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  if (num_splits == 0) num_splits = auto_splits(B, H, T, causal, pr.num_sms);
+  if (splitkv_bytes(B, H, T, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (fa::noalloc_scratch_address(&scratch) != cudaSuccess) {
     cudaGetLastError();
@@ -371,20 +400,24 @@ fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, vo
 }
 
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int T, int d, int num_splits) {
-  if (B < 1 || H < 1 || T < 1 || (d != 64 && d != 128) || num_splits < 1 || num_splits > FA_MAX_SPLITS) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * T;
-  const size_t bytes = static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 1) * 4;
-  return (bytes + 255) / 256 * 256;
+  if (B < 1 || H < 1 || T < 1 || (d != 64 && d != 128) || num_splits < 0 || num_splits > FA_MAX_SPLITS) return 0;
+  if (num_splits == 0) {  // the automatic choice, for either mask, on the current device
+    int dev = 0, sms = 0;
+    if (current_device(&dev, &sms) != FA_OK) return 0;
+    num_splits = std::max(auto_splits(B, H, T, 0, sms), auto_splits(B, H, T, 1, sms));
+  }
+  return splitkv_bytes(B, H, T, d, num_splits);
 }
 
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T,
                          int d, int causal, float scale, int num_splits, void* workspace, size_t workspace_bytes,
                          cudaStream_t stream) {
-  if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_BAD_ARG;
+  if (num_splits < 0 || num_splits > FA_MAX_SPLITS) return FA_ERR_BAD_ARG;
   Prepared pr;
   fa_status st = prepare(q, k, v, o, lse, B, H, H, T, d, causal, scale, &pr);
   if (st != FA_OK) return st;
-  const size_t need = fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits);
+  if (num_splits == 0) num_splits = auto_splits(B, H, T, causal, pr.num_sms);
+  const size_t need = splitkv_bytes(B, H, T, d, num_splits);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return FA_ERR_MISALIGNED;
   if ((st = check_device_range(workspace, need, pr.dev)) != FA_OK) return st;

@@ -108,7 +108,7 @@ struct Layout {
   static constexpr int ONES_BYTES = ONES ? 128 * 128 : (LSUM ? 16 * 128 : 0);
   static constexpr int BAR_OFF = ONES_OFF + ONES_BYTES;
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2],
-  // s_free[2], done
+  // (unused pair), done
   static constexpr int NUM_BARS = 4 + 2 * STAGES + 10 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // TMEM base slot, abort flag
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
@@ -205,6 +205,60 @@ __device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
+// Split-KV hand-off ("FlashAttention and Fused Kernels", section "Flash-Decoding": each split
+// yields a partial output and one log-sum-exp scalar per row; the partials are weighted by their
+// LSE).  Called by a whole warp after it has written the partials of its 32 rows [r0, r0 + 32)
+// of head bh for one split: the warp counts itself in that row group's counter, and the warp
+// that completes the count (the last split of the group to finish, in whatever CTA) merges the
+// group: with M = max_s LSE_s and w_s = e^(LSE_s - M),
+//   O = sum_s w_s O_s / sum_s w_s,   LSE = M + ln sum_s w_s,
+// over the n_run splits that hold a key these rows can see.  Lane c owns D/32 columns.
+template <int D>
+__device__ __noinline__ void split_handoff(const Params& p, int bh, int r0, int n_run, int lane) {
+  __threadfence();  // this warp's partials are visible device-wide before it is counted
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(p.counters + static_cast<size_t>(bh) * p.ngroups + r0 / 32, 1) == n_run - 1;
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();  // the other splits' partials, counted before this warp, are read after their fences
+  constexpr int CPL = D / 32;
+  const size_t rows = static_cast<size_t>(p.BH) * p.T;
+  for (int t = r0; t < min(r0 + 32, p.T); ++t) {
+    const size_t r = static_cast<size_t>(bh) * p.T + t;
+    float M = -INFINITY;
+    for (int s = 0; s < n_run; ++s) M = fmaxf(M, __ldcg(p.lsepart + s * rows + r));
+    float acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    float wsum = 0.f;
+    for (int s = 0; s < n_run; ++s) {
+      const float w = expf(__ldcg(p.lsepart + s * rows + r) - M);
+      wsum += w;
+      const float* src = p.opart + (s * rows + r) * D + lane * CPL;
+      if (CPL == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2 % CPL] += w * v.z;
+        acc[3 % CPL] += w * v.w;
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
+    const float inv = 1.f / wsum;
+    __nv_bfloat16* dst = p.o + r * D + lane * CPL;
+    if (CPL == 4) {
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2 % CPL] * inv, acc[3 % CPL] * inv));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0) p.lse[r] = M + logf(wsum);
+  }
+}
+
 template <int D, bool PARTIAL, bool F8 = false>
 __global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -227,10 +281,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t bar_p_full = barx + 16;   // [2]
   const uint32_t bar_o_full = barx + 32;   // [2]
   const uint32_t bar_o_empty = barx + 48;  // [2]
-  const uint32_t bar_s_free = barx + 64;   // [2] (SEP_P: S_i has been read into registers)
+  const uint32_t bar_s_free = barx + 64;   // [2] (SEP_P: one phase per S_i read, 4 arrivals)
   const uint32_t bar_done = barx + 80;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  // SEP_P: S reads of query tile i whose softmax step has ended, 4 per S (one per softmax warp of
+  // the tile); they guard the MMA warps' waits on s_free (see the MMA issuers)
+  const uint32_t s_reads = sbase + L::MISC_OFF + 8;  // [2] u32
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -254,6 +311,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     mbar_init(bar_done, L::MMA_WARPS);
     *abort_flag = 0;
+    reinterpret_cast<uint32_t*>(smem + L::MISC_OFF + 8)[0] = 0;
+    reinterpret_cast<uint32_t*>(smem + L::MISC_OFF + 8)[1] = 0;
     fence_mbar_init();
   }
   if (warp == MMA_WARP0) {
@@ -414,9 +473,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     //
     // The two tiles' S products share one Tensor Memory buffer and take it in turn: per K/V
     // step S_0(x), then S_1(x) (a tile past its last step drops out), unit after unit.  A
-    // product is issued once the softmax has read the one before it in that order, which
-    // s_free[t] reports for tile t (it completes once per S_t read).  Because the products
-    // are strictly ordered, the awaited completion is always the next one of that barrier.
+    // product is issued once the softmax has read the one before it in that order.  Each read
+    // of S_t is recorded twice: the four softmax warps of tile t arrive on s_free[t] (one phase
+    // per read) right after it, and add one each to the counter s_reads[t] (release) at the
+    // end of that step.  A warp may come to wait
+    // for a read two or more reads ahead of tile t's progress (for instance the first S of its
+    // next unit while the other tile still has two products to go), and an mbarrier's phase
+    // parity cannot tell that apart from a completed phase; so the MMA warp first waits
+    // (acquire) until the counter shows every earlier read of tile t, and only then waits on
+    // the phase of the read it needs, which is then the barrier's current or completed one.
     {
       const int i = warp - MMA_WARP0;  // query tile of this warp
       constexpr uint32_t IDESC_S = F8 ? make_idesc_e4m3(BM, BN) : make_idesc_bf16(BM, BN, 0);  // both K-major
@@ -471,6 +536,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       pt = last_t, pk = (last_t ? cnt1 : cnt0) - 1;                                                     \
     }                                                                                                   \
     if (pt >= 0) {                                                                                      \
+      if (!(ok = wait_count_all(W, s_reads + 4 * pt, 4u * uint32_t(pk)))) break;                         \
       if (!(ok = wait_all(W, bar_s_free + 8 * pt, uint32_t(pk) & 1u))) break;                           \
       tc_fence_after();                                                                                 \
     }                                                                                                   \
@@ -716,7 +782,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t t_s = tmem + lane_off + L::s_col(i);
     const uint32_t t_o = tmem + lane_off + L::o_col(i);
     const uint32_t t_p = tmem + lane_off + L::p_col(i);
-    const uint32_t my_s_full = bar_s_full + 8 * i, my_p_full = bar_p_full + 8 * i, my_s_free = bar_s_free + 8 * i;
+    const uint32_t my_s_full = bar_s_full + 8 * i, my_p_full = bar_p_full + 8 * i, my_s_reads = s_reads + 4 * i;
+    const uint32_t my_s_free = bar_s_free + 8 * i;
     const uint32_t my_o_full = bar_o_full + 8 * i, my_o_empty = bar_o_empty + 8 * i;
     const float sl2 = p.scale_log2;
     const uint32_t stg = sbase + L::STG_OFF + warp * L::STG_WARP_BYTES;  // this warp's O staging
@@ -859,7 +926,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(my_p_full);
+        if (lane == 0) {
+          // counted at the end of the step (release: after this read's s_free arrival), off the path
+          // from the S read to the next S product; the count guards the MMA warps' s_free waits
+          if (L::SEP_P) smem_count_add_release(my_s_reads, 1u);
+          mbar_arrive(my_p_full);
+        }
       }
       if (!ok) break;
       // epilogue: O = o / lr in bf16, LSE = ln(2) (m + log2 l)
@@ -886,6 +958,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
         }
         if (row < p.T) p.lsepart[prow] = (m_run + log2f(l)) * LN2;
+        const int r0 = q0 + wq * 32;
+        if (r0 < p.T)  // splits that hold a key of this query tile: every one before its last visible key tile
+          split_handoff<D>(p, u.bh, r0, p.causal ? min(p.num_splits, (q0 / BN) / p.split_tiles + 1) : p.num_splits,
+                           lane);
       } else {
         // O in bf16 through shared memory: the warp's 32 rows x 64 columns in the 128-byte
         // swizzled layout of the output map (16-byte chunk c of row r at chunk c ^ (r % 8), so
@@ -1085,68 +1161,6 @@ cudaError_t launch_fa_fwd_partial(int d, const CUtensorMap& q, const CUtensorMap
                                   const Params& p, int grid, cudaStream_t stream) {
   if (d == 64) return launch<64, true>(q, k, v, q, p, grid, stream);
   return launch<128, true>(q, k, v, q, p, grid, stream);
-}
-
-// Merge of the per-split partials of every row ("FlashAttention and Fused
-// Kernels", section "Flash-Decoding": each split's output is weighted by its
-// log-sum-exp): with M = max_s LSE_s and w_s = e^(LSE_s - M),
-//   O = sum_s w_s O_s / sum_s w_s,   LSE = M + ln sum_s w_s.
-// A split contributes to row t when its first key is visible to t (causal) or
-// lies before T.  One warp per row; lane c owns D/32 contiguous columns.
-template <int D>
-__global__ void __launch_bounds__(256) fa_split_combine_kernel(const Params p) {
-  constexpr int CPL = D / 32;  // columns per lane
-  const int lane = threadIdx.x % 32;
-  const size_t rows = static_cast<size_t>(p.BH) * p.T;
-  const size_t warps = gridDim.x * (blockDim.x / 32);
-  const int tiles_total = (p.nk + p.split_tiles - 1) / p.split_tiles;
-  for (size_t r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < rows; r += warps) {
-    const int t = static_cast<int>(r % p.T);
-    int ns = min(p.num_splits, tiles_total);
-    if (p.causal) ns = min(ns, t / (BN * p.split_tiles) + 1);
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, p.lsepart[s * rows + r]);
-    float acc[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-    float wsum = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float w = expf(p.lsepart[s * rows + r] - M);
-      wsum += w;
-      const float* src = p.opart + (s * rows + r) * D + lane * CPL;
-      if (CPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2 % CPL] += w * v.z;
-        acc[3 % CPL] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-      }
-    }
-    const float inv = 1.f / wsum;
-    __nv_bfloat16* dst = p.o + r * D + lane * CPL;
-    if (CPL == 4) {
-      uint2 pk = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2 % CPL] * inv, acc[3 % CPL] * inv));
-      *reinterpret_cast<uint2*>(dst) = pk;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    }
-    if (lane == 0) p.lse[r] = M + logf(wsum);
-  }
-}
-
-cudaError_t launch_split_combine(int d, const Params& p, int num_sms, cudaStream_t stream) {
-  const size_t rows = static_cast<size_t>(p.BH) * p.T;
-  const size_t blocks_needed = (rows + 7) / 8;
-  const int grid = static_cast<int>(blocks_needed < static_cast<size_t>(num_sms) * 8 ? blocks_needed : num_sms * 8);
-  if (d == 64)
-    fa_split_combine_kernel<64><<<grid, 256, 0, stream>>>(p);
-  else
-    fa_split_combine_kernel<128><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- fixed scratch (no allocation)

@@ -33,6 +33,8 @@ struct Params {
   int split_tiles;            // key tiles per split (>= 1)
   float* opart;               // [num_splits][BH*T][d] fp32 partial outputs (normalised)
   float* lsepart;             // [num_splits][BH*T] fp32 partial LSE (natural log)
+  int* counters;              // [BH][ngroups] splits finished per 32-row group (zero at launch)
+  int ngroups;                // ceil(T / 32)
 };
 
 // Rows per box of the output tensor map `o` (bf16 (d, T, B*H), 128-byte swizzle): each
@@ -46,10 +48,11 @@ cudaError_t launch_fa_fwd_e4m3(const CUtensorMap& q, const CUtensorMap& k, const
 // V (B*H, T, 128) e4m3 -> V^T (B*H, 128, Tp) with keys Tp > T zero (Tp = T rounded up to 16).
 cudaError_t launch_transpose_e4m3(const void* v, void* vt, int BH, int T, int Tp, cudaStream_t stream);
 int fa_fwd_e4m3_smem_bytes();
-// The same kernel writing per-split partials (p.opart, p.lsepart), then the merge.
+// The same kernel over (query block, key split) units: each split writes its partials
+// (p.opart, p.lsepart), and the last split of every 32-row group to finish merges the group
+// into O and LSE (p.counters must be zero at launch).
 cudaError_t launch_fa_fwd_partial(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                   const Params& p, int grid, cudaStream_t stream);
-cudaError_t launch_split_combine(int d, const Params& p, int num_sms, cudaStream_t stream);
 int fa_fwd_smem_bytes(int d);
 int fa_fwd_threads(int d);
 int fa_fwd_rows_per_unit();

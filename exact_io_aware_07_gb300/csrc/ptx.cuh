@@ -46,6 +46,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Monotonic shared-memory counters (release add, acquire load).  Unlike an mbarrier's phase
+// parity, a counter can be waited on for any future value without aliasing.
+__device__ __forceinline__ void smem_count_add_release(uint32_t addr, uint32_t v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t smem_count_load_acquire(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
@@ -477,6 +488,28 @@ struct Waiter {
     }
   }
 };
+
+// Bounded wait until the counter at `addr` reaches `target` (same limits and abort handling as
+// Waiter::wait); the whole warp calls it and agrees on the outcome.
+static __device__ __noinline__ bool wait_count_slow(const Waiter& W, uint32_t addr, uint32_t target) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (smem_count_load_acquire(addr) >= target) return true;
+    __nanosleep(64);  // leave the issue slots to the warps that will move the count
+    if ((it & 31u) == 0) {
+      if (*W.abort_flag) return false;
+      if (globaltimer_ns() - t0 > W.limit_ns) {
+        *W.abort_flag = 1;
+        atomicOr(W.status, 1u);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool wait_count_all(const Waiter& W, uint32_t addr, uint32_t target) {
+  const bool done = smem_count_load_acquire(addr) >= target || wait_count_slow(W, addr, target);
+  return __all_sync(0xffffffffu, done);
+}
 
 // Warp-wide forms for the issuing warps: every lane waits, and the warp agrees on
 // the outcome (a lane that timed out makes the whole warp give up).

@@ -105,17 +105,23 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
  * separate work units (Flash-Decoding: "FlashAttention and Fused Kernels:
  * Attention Without the n x n Matrix", section "Flash-Decoding: split the
  * cache, not the queries").  Each unit writes its range's normalised output
- * (fp32) and log-sum-exp into `workspace`; a second kernel on the same stream
- * merges them, weighting each split by its log-sum-exp.  O and LSE are the
+ * (fp32) and log-sum-exp into `workspace`; in the same launch, the last split
+ * of every group of 32 query rows to finish merges that group, weighting each
+ * split by its log-sum-exp (a counter per group in the workspace, cleared by
+ * an asynchronous memset on `stream` before the launch).  O and LSE are the
  * same quantities fa_fwd computes (up to rounding).
  *   q .. scale, stream : as for fa_fwd.
  *   num_splits : 1 .. FA_MAX_SPLITS; the keys (ceil(T / 128) tiles of 128) are
  *                cut into ceil(tiles / ceil(tiles / num_splits)) ranges of
- *                equal tile count.
+ *                equal tile count.  0 chooses the count: enough splits that
+ *                the longest unit's share of the keys fits in the average work
+ *                per SM of the current device, at most 16 (1 when the work
+ *                units alone balance the SMs).
  *   workspace  : caller-owned device memory of at least
  *                fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) bytes,
  *                16-byte aligned, not overlapping any tensor argument.  Its
- *                contents are scratch: overwritten, never read before written.
+ *                contents are scratch: overwritten, never read before written
+ *                (the counters are cleared by the call itself).
  * Errors: as fa_fwd, plus FA_ERR_BAD_ARG (num_splits out of range) and
  * FA_ERR_WORKSPACE (NULL or too small a workspace).
  */
@@ -229,8 +235,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int T);
  *
  * Arguments and results are those of fa_fwd_splitkv minus the workspace.
  * Limits and behaviour:
- *   - fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) must not exceed
- *     FA_NOALLOC_SCRATCH_BYTES, else FA_ERR_WORKSPACE and nothing runs;
+ *   - the scratch that the call needs (fa_fwd_splitkv_workspace_bytes for the
+ *     split count it uses; num_splits = 0 chooses it as fa_fwd_splitkv does)
+ *     must not exceed FA_NOALLOC_SCRATCH_BYTES, else FA_ERR_WORKSPACE and
+ *     nothing runs;
  *   - the first call on each device looks up the scratch's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture on that device.  The
@@ -239,8 +247,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int T);
  *     current, the next call looks it up again (the cache is keyed on the
  *     context's unique id), and that call too should precede any capture;
  *   - every call on a device shares the one scratch array, which keeps what
- *     the last call left there.  Nothing in it needs to start at zero: each
- *     call writes every partial before its merge reads it.  Calls whose
+ *     the last call left there.  The only part that must start at zero, the
+ *     merge counters, is cleared by each call (an asynchronous memset on
+ *     `stream`); every partial is written before the merge reads it.  Calls whose
  *     kernels overlap on the GPU (different streams without ordering between
  *     them) race on the scratch and give wrong results; order them.
  */
@@ -248,7 +257,12 @@ fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, vo
                                  int B, int H, int T, int d, int causal, float scale, int num_splits,
                                  cudaStream_t stream);
 
-/* Workspace bytes fa_fwd_splitkv needs (0 for invalid sizes): num_splits * B*H*T * (d + 1) * 4, rounded up to 256. */
+/*
+ * Workspace bytes fa_fwd_splitkv needs (0 for invalid sizes):
+ * num_splits * B*H*T * (d + 1) * 4 + B*H*ceil(T / 32) * 4, rounded up to 256.
+ * num_splits = 0: the size for the count the call would choose on the current
+ * device (the larger of the causal and non-causal choices).
+ */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int T, int d, int num_splits);
 
 /* A static, human-readable name for a status code. */

@@ -99,13 +99,15 @@ def test_selftest_rejects_bad_timeout(lib):
 
 
 def test_splitkv_workspace_size(lib):
-    assert fa.fa_fwd_splitkv_workspace_bytes(1, 4, 256, 64, 2) == (2 * 4 * 256 * 65 * 4 + 255) // 256 * 256
-    assert fa.fa_fwd_splitkv_workspace_bytes(2, 3, 1000, 128, 7) == (7 * 6 * 1000 * 129 * 4 + 255) // 256 * 256
-    for bad in ((0, 1, 1, 64, 1), (1, 1, 1, 96, 1), (1, 1, 1, 64, 0), (1, 1, 1, 64, fa.FA_MAX_SPLITS + 1)):
+    # partial outputs and LSE of every split, then one counter per 32 query rows of every head
+    assert fa.fa_fwd_splitkv_workspace_bytes(1, 4, 256, 64, 2) == (2 * 4 * 256 * 65 * 4 + 4 * 8 * 4 + 255) // 256 * 256
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 3, 1000, 128, 7) == \
+        (7 * 6 * 1000 * 129 * 4 + 6 * 32 * 4 + 255) // 256 * 256
+    for bad in ((0, 1, 1, 64, 1), (1, 1, 1, 96, 1), (1, 1, 1, 64, -1), (1, 1, 1, 64, fa.FA_MAX_SPLITS + 1)):
         assert fa.fa_fwd_splitkv_workspace_bytes(*bad) == 0
 
 
-@pytest.mark.parametrize("ns,ws,code", [(0, A + 0x5000, 9), (fa.FA_MAX_SPLITS + 1, A + 0x5000, 9)])
+@pytest.mark.parametrize("ns,ws,code", [(-1, A + 0x5000, 9), (fa.FA_MAX_SPLITS + 1, A + 0x5000, 9)])
 def test_splitkv_host_validation(lib, ns, ws, code):
     rc = lib.fa_fwd_splitkv(A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 1, 2, 128, 64, 0,
                             ctypes.c_float(0.125), ns, ws, 1 << 20, None)

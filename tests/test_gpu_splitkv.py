@@ -68,6 +68,47 @@ def test_splitkv_workloads(name, num_splits):
             bound=rounding_bound(q64, k64, v64, w["causal"], scale))
 
 
+@pytest.mark.parametrize("B,H,T,d,causal", [(1, 4, 8192, 128, 1), (1, 4, 256, 64, 1), (1, 2, 3000, 64, 0)])
+def test_splitkv_automatic_count(B, H, T, d, causal):
+    """num_splits = 0: the library picks the count (few work units, long rows: more than one split)."""
+    import torch
+
+    import exact_io_aware_07_gb300 as fa
+
+    qkv = fi.make_qkv(B, H, T, d, seed=23)
+    scale = default_scale(d)
+    o, lse = _run_split(qkv, causal, scale, 0)
+    q64, k64, v64 = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    O_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, causal, scale)
+    compare(o, lse, O_ref, lse_ref, label=f"split-auto B{B} H{H} T{T} d{d} causal{causal}",
+            bound=rounding_bound(q64, k64, v64, causal, scale))
+    nk = (T + 127) // 128
+    assert fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, 0) >= fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, 1)
+    if (B, H, T) == (1, 4, 8192):  # 128 units of work for 152 SMs, the longest 64 key tiles long
+        assert fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, 0) > fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, 1)
+    assert nk >= 1 and torch.cuda.is_available()
+
+
+def test_splitkv_reused_workspace_and_repeatable():
+    """The counters are cleared by every call: a workspace reused across calls (and shapes) gives the same bits."""
+    import torch
+
+    import exact_io_aware_07_gb300 as fa
+
+    ws = torch.full((fa.fa_fwd_splitkv_workspace_bytes(2, 3, 1000, 128, 4),), 0x7F, dtype=torch.uint8, device="cuda")
+    outs = []
+    for T, seed in ((1000, 24), (700, 25), (1000, 24)):
+        qkv = fi.make_qkv(2, 3, T, 128, seed=seed)
+        q, k, v = (to_device(None, b) for b in (qkv.q_bits, qkv.k_bits, qkv.v_bits))
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+        fa.fa_fwd_splitkv(q, k, v, o, lse, True, default_scale(128), 4, ws)
+        outs.append((o, lse))
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert torch.equal(outs[0][0].view(torch.int16), outs[2][0].view(torch.int16)) and torch.equal(outs[0][1], outs[2][1])
+
+
 def test_splitkv_rejects_bad_workspace():
     import ctypes
 
