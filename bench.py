@@ -72,13 +72,30 @@ def load_peaks():
 
 
 def library_fingerprint():
+    """Hash of the library's sources and build flags (identifies the build a number was taken on)."""
     from exact_io_aware_07_gb300 import _build
 
     return _build._fingerprint(())[:16]
 
 
+def forward_fingerprint():
+    """Hash of the sources that make up the forward kernel and its launch (the backward kernels'
+    source is left out), so that recorded ncu traffic of the forward kernel stays matched while
+    only the backward changes."""
+    import hashlib
+
+    from exact_io_aware_07_gb300 import _build
+
+    h = hashlib.sha256()
+    for name in ("fa_kernel.cu", "fa_kernel.h", "ptx.cuh", "fa_api.cu"):
+        with open(os.path.join(_build.CSRC, name), "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(_build.ARCH + _build.CFLAGS).encode())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(workload, fingerprint):
-    """DRAM bytes per launch from an ncu summary under profiles/, if taken on this kernel build.
+    """DRAM bytes per launch from an ncu summary under profiles/, if taken on this forward-kernel build.
 
     Returns (bytes, file name) or (None, None).  The figure is dram__bytes_read.sum +
     dram__bytes_write.sum of one launch in a separate ncu capture of the same library build
@@ -282,13 +299,13 @@ def run_ours(args, world, rank, local, pg):
     value = world * K * f_step / total_s / 1e12
     achieved = f_step / launch_s / 1e12
     fp = library_fingerprint()
-    traffic, traffic_file = recorded_traffic(name, fp)
+    traffic, traffic_file = recorded_traffic(name, forward_fingerprint())
     roofline = {
         "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
         "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
-        "traffic_source": (f"ncu capture of one launch of this library build (dram__bytes_read.sum + "
+        "traffic_source": (f"ncu capture of one launch of this forward-kernel build (dram__bytes_read.sum + "
                            f"dram__bytes_write.sum), profiles/{traffic_file}") if traffic else
-                          "no ncu capture of this library build on record",
+                          "no ncu capture of this forward-kernel build on record",
         "peak_source": f"{peak_src} bf16 burst", "kernel": "fa_fwd_kernel",
         "floor_bytes": floor_bytes(B, H, T, d),
         "attainable_tflops": round(min(peaks["bf16_tflops"],
@@ -325,7 +342,7 @@ def run_ours(args, world, rank, local, pg):
         "config": workload_config(name, w, world),
         "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
         "roofline": roofline, "e2e": e2e, "gpu_launches": K, "clocks": clk, "cpu_baseline": cpu,
-        "parity": parity, "library_fingerprint": fp,
+        "parity": parity, "library_fingerprint": fp, "forward_kernel_fingerprint": forward_fingerprint(),
     }
     if sweep is not None:
         line["sweep"] = sweep
