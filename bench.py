@@ -45,7 +45,7 @@ SWEEP_DEFAULT = ["tiny_causal_b1h4t256d64", "gpt2s_causal_b8h12t1024d64", "gpt2m
 # with fewer work units than SMs, where one head's long rows would otherwise leave SMs idle
 SPLITKV_SWEEP = {"splitkv_tiny_causal_b1h4t256d64": dict(B=1, H=4, T=256, d=64, causal=True),
                  "splitkv_prefill_causal_b1h4t8192d128": dict(B=1, H=4, T=8192, d=128, causal=True),
-                 "splitkv_prefill_b1h2t16384d64": dict(B=1, H=2, T=16384, d=64, causal=False)}
+                 "splitkv_single_causal_b1h1t32768d128": dict(B=1, H=1, T=32768, d=128, causal=True)}
 # grouped K/V heads: Llama-3.1-8B attention (32 query heads sharing 8 K/V heads), causal and not
 GQA_SWEEP = {"llama8b_gqa_causal_b1h32kv8t4096d128": dict(B=1, H=32, Hkv=8, T=4096, d=128, causal=True),
              "llama8b_gqa_b1h32kv8t4096d128": dict(B=1, H=32, Hkv=8, T=4096, d=128, causal=False)}
@@ -622,6 +622,7 @@ def run_sweep(fa, torch, dev, names, peaks, splitkv=SPLITKV_SWEEP, gqa=GQA_SWEEP
                      "tflops_unsplit": round(f / sec["unsplit"] / 1e12, 1),
                      "speedup": round(sec["unsplit"] / sec["split"], 3), "steps": steps, "workspace_bytes": ws_bytes,
                      "num_splits": "chosen by the library (0)",
+                     "key_ranges_used": fa.fa_fwd_splitkv_count(g["B"], g["H"], g["T"], g["d"], g["causal"], 0),
                      "kernels": "fa_fwd_kernel (partial, last split of each 32-row group merges) vs fa_fwd_kernel"}
         torch.cuda.empty_cache()
     for name in names:

@@ -14,7 +14,7 @@ Entry points (same names as the C ABI):
     fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, workspace, stream=None)
     fa_fwd_splitkv_noalloc(q, k, v, o, lse, causal, scale, num_splits, stream=None)
     fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale, workspace, stream=None)
-    fa_fwd_splitkv_workspace_bytes, fa_fwd_fp8_workspace_bytes, fa_bwd_workspace_bytes
+    fa_fwd_splitkv_workspace_bytes, fa_fwd_splitkv_count, fa_fwd_fp8_workspace_bytes, fa_bwd_workspace_bytes
     fa_status_string(code), fa_device_status(stream=None), fa_selftest_wait_timeout(us, stream=None)
     fa_fwd_launch_shape(B, H, T, d, causal, num_sms), fa_ex2_rate(stream=None), fa_version()
 and the convenience wrappers ``attention``, ``attention_gqa``, ``attention_splitkv``
@@ -30,7 +30,7 @@ from ._build import build, lib_path  # noqa: F401
 
 __all__ = [
     "FAError", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
-    "fa_status_string", "fa_device_status", "FA_NOALLOC_SCRATCH_BYTES",
+    "fa_fwd_splitkv_count", "fa_status_string", "fa_device_status", "FA_NOALLOC_SCRATCH_BYTES",
     "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_ex2_rate", "fa_version",
     "attention", "attention_splitkv", "load_library", "STATUS", "FA_MAX_SPLITS",
 ]
@@ -44,7 +44,7 @@ STATUS = {
 FA_MAX_SPLITS = 256
 EXPORTED = ["fa_fwd", "fa_fwd_gqa", "fa_fwd_paged", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_bwd",
             "fa_bwd_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_workspace_bytes",
-            "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_ex2_rate",
+            "fa_fwd_splitkv_count", "fa_status_string", "fa_device_status", "fa_fwd_launch_shape", "fa_selftest_wait_timeout", "fa_ex2_rate",
             "fa_version"]
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -97,6 +97,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd_splitkv_noalloc.restype = i
     lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_fwd_splitkv_count.argtypes = [i, i, i, i, i, i]
+    lib.fa_fwd_splitkv_count.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
@@ -325,6 +327,11 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, causal, scale, stream)
     return o, lse
+
+
+def fa_fwd_splitkv_count(B: int, H: int, T: int, d: int, causal: bool, num_splits: int) -> int:
+    """Key ranges ``fa_fwd_splitkv`` would use (``num_splits`` 0: the library's choice); -1 if invalid."""
+    return int(load_library().fa_fwd_splitkv_count(B, H, T, d, int(bool(causal)), num_splits))
 
 
 def fa_fwd_splitkv_workspace_bytes(B: int, H: int, T: int, d: int, num_splits: int) -> int:

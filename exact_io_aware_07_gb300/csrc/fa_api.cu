@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <vector>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -247,18 +249,108 @@ fa_status prepare(const void* q, const void* k, const void* v, void* o, float* l
   return FA_OK;
 }
 
-// Key splits chosen for num_splits == 0: enough that the longest unit's share of the keys fits in
-// the average work per SM (units of 256 query rows, work counted in 128-key tiles), at most 16;
-// 1 when the units alone fill the SMs evenly enough.
+// Key splits chosen for num_splits == 0.  The persistent grid's static schedule is replayed on
+// the host for 1 .. 16 splits (the kernel's unit list and its snake assignment of units to
+// CTAs; a unit costs the K/V steps of its longer query tile plus kUnitSteps for its start and
+// epilogue, plus kMergeSteps when it holds the last key tile of its rows and so may merge
+// them; a split launch adds kLaunchSteps), and the count with the least busiest-CTA total wins
+// if it beats the unsplit launch by at least 10 %.  The costs are in 128-key steps and were
+// fitted to split and unsplit timings on GB300 (B = 1-2, H = 1-32, T = 256-32768, d = 64 and
+// 128, causal and not).  Larger problems (more than 16 K units) are not split: their units
+// already spread over the SMs.  Results are cached per shape, so that only the first call of a
+// shape pays for the replay.
+int auto_splits_uncached(int B, int H, int T, int causal, int num_sms) {
+  constexpr double kUnitSteps = 2.0, kMergeSteps = 10.0, kLaunchSteps = 2.0;
+  const long long BH = static_cast<long long>(B) * H;
+  const int nk = (T + 127) / 128, nqb = (T + 255) / 256;
+  if (BH * nqb > 16384) return 1;
+  std::vector<double> load;
+  auto makespan = [&](int want) -> double {
+    const int st = (nk + want - 1) / want, ns = (nk + st - 1) / st;
+    const long long units = BH * nqb * ns;
+    const long long G = std::min<long long>(units, num_sms);
+    load.assign(static_cast<size_t>(G), 0.0);
+    for (long long w = 0; w < units; ++w) {
+      const long long k = w / G, pos = w - k * G;
+      const long long b = (k & 1) ? G - 1 - pos : pos;
+      int band, sp = 0;
+      if (ns > 1) {  // (band, split, head), as the kernel's split form lists them
+        band = static_cast<int>(w / (BH * ns));
+        sp = static_cast<int>((w - band * BH * ns) / BH);
+      } else {  // causal: band by band; otherwise head by head
+        band = static_cast<int>(causal ? w / BH : w % nqb);
+      }
+      const int qb = causal ? nqb - 1 - band : band;
+      const int q0 = qb * 256, q1 = q0 + 128;
+      const int e0 = q0 >= T ? 0 : (causal ? std::min(nk, q0 / 128 + 1) : nk);
+      const int e1 = q1 >= T ? 0 : (causal ? std::min(nk, q1 / 128 + 1) : nk);
+      const int lo = sp * st, hi = lo + st;
+      const int n = std::max(std::max(0, std::min(e0, hi) - lo), std::max(0, std::min(e1, hi) - lo));
+      if (n == 0) continue;
+      double c = n + kUnitSteps;
+      if (ns > 1 && std::max(e0, e1) <= hi) c += kMergeSteps;
+      load[static_cast<size_t>(b)] += c;
+    }
+    return *std::max_element(load.begin(), load.end()) + (ns > 1 ? kLaunchSteps : 0.0);
+  };
+  const double t1 = makespan(1);
+  double best = t1;
+  int best_s = 1;
+  for (int sp = 2; sp <= std::min(nk, 16); ++sp) {
+    const double t = makespan(sp);
+    if (t < best) {
+      best = t;
+      best_s = sp;
+    }
+  }
+  return best <= 0.9 * t1 ? best_s : 1;
+}
+
 int auto_splits(int B, int H, int T, int causal, int num_sms) {
-  const long long nk = (T + 127) / 128, nqb = (T + 255) / 256;
-  long long work = 0;  // K/V tiles over all units
-  for (long long qb = 0; qb < nqb; ++qb) work += causal ? std::min(nk, 2 * qb + 2) : nk;
-  work *= static_cast<long long>(B) * H;
-  const double per_sm = static_cast<double>(work) / num_sms;
-  const long long longest = causal ? std::min(nk, 2 * nqb) : nk;
-  long long s = per_sm >= 1.0 ? static_cast<long long>(std::ceil(longest / per_sm)) : longest;
-  return static_cast<int>(std::max(1LL, std::min({s, nk, 16LL})));
+  struct Entry {
+    int B, H, T, causal, sms, splits;
+  };
+  static Entry cache[64] = {};
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+      const Entry& e = cache[i];
+      if (e.B == B && e.H == H && e.T == T && e.causal == causal && e.sms == num_sms) return e.splits;
+    }
+  }
+  const int s = auto_splits_uncached(B, H, T, causal, num_sms);
+  std::lock_guard<std::mutex> lock(mu);
+  Entry& e = used < 64 ? cache[used++] : cache[next++ % 64];
+  e = Entry{B, H, T, causal, num_sms, s};
+  return s;
+}
+
+// Order of the work items of an unsplit launch.  Causal bf16 d = 128 launches whose K and V
+// (one K/V head per query head) exceed 96 MB over all heads, so that L2 cannot hold what the
+// CTAs running at one time stream when every head is in flight: the units are listed band by
+// band within groups of heads whose K and V fit in 48 MB, and claimed at run time from one of
+// the library's counter pairs (taken in turn), so that the CTAs running at one time work on
+// one or two groups' heads while claiming in list order keeps the longest units first and the
+// SMs evenly loaded.  Every other launch keeps the static band-by-band (causal) or head-by-head
+// order.  If the counters cannot be found the static order is kept.
+void choose_order(fa::Params& p, int d, int group) {
+  p.head_group = 0;
+  p.sched = nullptr;
+  if (!p.causal || d != 128 || group != 1) return;
+  const double head_kv = static_cast<double>(p.T) * d * 2 * 2;  // bytes of K and V of one head
+  if (head_kv * p.BH <= 96e6) return;
+  int g = std::max(1, std::min(p.BH, static_cast<int>(48e6 / head_kv)));
+  while (p.BH % g != 0) --g;
+  int* base = nullptr;
+  if (fa::sched_counters_address(&base) != cudaSuccess || !base) {
+    cudaGetLastError();
+    return;
+  }
+  static std::atomic<unsigned> seq{0};
+  p.sched = base + static_cast<size_t>(seq.fetch_add(1) % fa::kSchedSlots) * fa::kSchedStride;
+  p.head_group = g;
 }
 
 // Workspace layout of the split form: [splits][B*H*T][d] fp32 partial outputs, [splits][B*H*T]
@@ -277,6 +369,14 @@ fa_status launch_splitkv(Prepared& pr, int d, int num_splits, float* ws, cudaStr
   fa::Params& p = pr.p;
   p.split_tiles = (p.nk + num_splits - 1) / num_splits;
   p.num_splits = (p.nk + p.split_tiles - 1) / p.split_tiles;  // every split holds at least one key tile
+  if (p.num_splits == 1) {  // one split is the plain launch: no partials, nothing to merge
+    const int grid = p.num_units < pr.num_sms ? p.num_units : pr.num_sms;
+    if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, pr.to, p, grid, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
+    return FA_OK;
+  }
   const size_t rows = static_cast<size_t>(p.BH) * p.T;
   p.opart = ws;
   p.lsepart = ws + static_cast<size_t>(p.num_splits) * rows * d;
@@ -308,6 +408,7 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
   Prepared pr;
   fa_status st = prepare(q, k, v, o, lse, B, H, Hkv, T, d, causal, scale, &pr);
   if (st != FA_OK) return st;
+  choose_order(pr.p, d, H / Hkv);
   const int grid = pr.p.num_units < pr.num_sms ? pr.p.num_units : pr.num_sms;
   if (fa::launch_fa_fwd(d, pr.tq, pr.tk, pr.tv, pr.to, pr.p, grid, stream) != cudaSuccess) {
     cudaGetLastError();
@@ -407,6 +508,19 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int T, int d, int num_splits
     num_splits = std::max(auto_splits(B, H, T, 0, sms), auto_splits(B, H, T, 1, sms));
   }
   return splitkv_bytes(B, H, T, d, num_splits);
+}
+
+int fa_fwd_splitkv_count(int B, int H, int T, int d, int causal, int num_splits) {
+  if (B < 1 || H < 1 || T < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1) || num_splits < 0 ||
+      num_splits > FA_MAX_SPLITS)
+    return -1;
+  if (num_splits == 0) {
+    int dev = 0, sms = 0;
+    if (current_device(&dev, &sms) != FA_OK) return -1;
+    num_splits = auto_splits(B, H, T, causal, sms);
+  }
+  const int nk = (T + 127) / 128, st = (nk + num_splits - 1) / num_splits;
+  return (nk + st - 1) / st;
 }
 
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T,

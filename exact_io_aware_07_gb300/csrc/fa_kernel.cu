@@ -108,10 +108,11 @@ struct Layout {
   static constexpr int ONES_BYTES = ONES ? 128 * 128 : (LSUM ? 16 * 128 : 0);
   static constexpr int BAR_OFF = ONES_OFF + ONES_BYTES;
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2],
-  // (unused pair), done
-  static constexpr int NUM_BARS = 4 + 2 * STAGES + 10 + 1;
-  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // TMEM base slot, abort flag
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
+  // s_free[2], done, unit_full[4], unit_empty[4]
+  static constexpr int NUM_BARS = 4 + 2 * STAGES + 10 + 1 + 8;
+  // TMEM base slot, abort flag, S-read counters [2], claimed work items [4]
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 32 + 1024;  // + slack to align the base to 1 KB
   // Tensor Memory columns.  bf16 d = 128: S_0 [0,128), S_1 [128,256), O_0, O_1 after them, P_i
   // over S_i.  d = 64: one S buffer [0,128) that the two query tiles' products take in turn,
   // O_0 [128,208) and O_1 [224,304) (64 columns of O and 16 of the weight sum each),
@@ -151,7 +152,7 @@ struct Unit {
 // time then share a few heads' K and V, which stay in L2.  With split keys,
 // split s of a unit covers key tiles [s * split_tiles, (s + 1) * split_tiles)
 // of what each query tile may see.
-template <bool PARTIAL>
+template <bool PARTIAL, bool GROUPED>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
   Unit u;
   int band, s = 0;
@@ -161,6 +162,11 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
     const int rem = w - band * per_band;
     s = rem / p.BH;
     u.bh = rem - s * p.BH;
+  } else if (GROUPED && p.head_group > 0) {  // causal: band by band within each group of head_group heads
+    const int per_group = p.head_group * p.nqb;
+    const int g = w / per_group, r = w - g * per_group;
+    band = r / p.head_group;
+    u.bh = g * p.head_group + (r - band * p.head_group);
   } else {  // one division: w = first * unit_div + second
     const int first = w / p.unit_div, second = w - first * p.unit_div;
     band = p.causal ? first : second;
@@ -202,6 +208,26 @@ __device__ __forceinline__ void balance_slots(Unit& u, int& bal) {
 // (b, 2G-1-b, 2G+b, ...), which pairs long causal units with short ones.
 __device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k & 1) ? (G - 1 - b) : b); }
 
+// Claimed work items (p.sched != nullptr): a CTA's first item is blockIdx.x; every later one is
+// claimed by the producer warp from the counter pair (item G + the counter's previous value,
+// so that the list is worked through in order, each CTA taking the next item whenever it is
+// ready for one) and handed to the other warps through a ring of four shared-memory slots:
+// item k (k >= 1) goes through slot (k - 1) % 4, whose unit_full barrier the producer
+// completes after writing it and whose unit_empty barrier the readers (softmax and MMA warps)
+// complete after reading it.  Returns item k for a reading warp, or -1 when the producer has
+// handed out an index past the last unit (or a wait ran out: ok = false).
+__device__ __forceinline__ int claimed_item(const Params& p, const Waiter& W, uint32_t slots, uint32_t full,
+                                            uint32_t empty, int k, bool& ok) {
+  if (k == 0) return blockIdx.x;
+  const int j = k - 1, s = j & 3;
+  if (!(ok = wait_all(W, full + 8 * s, (j >> 2) & 1))) return -1;
+  int w;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(w) : "r"(slots + 4 * s) : "memory");
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty + 8 * s);
+  return w < p.num_units ? w : -1;
+}
+
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
@@ -212,7 +238,11 @@ __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 // that completes the count (the last split of the group to finish, in whatever CTA) merges the
 // group: with M = max_s LSE_s and w_s = e^(LSE_s - M),
 //   O = sum_s w_s O_s / sum_s w_s,   LSE = M + ln sum_s w_s,
-// over the n_run splits that hold a key these rows can see.  Lane c owns D/32 columns.
+// over the n_run splits that hold a key these rows can see.  Lane l takes the LSE of row
+// r0 + l (M, the weight sum, and each split's weight, handed to the other lanes by shuffle);
+// the rows' outputs are formed eight rows at a time with every lane holding D / 32 columns,
+// so that eight rows of a split (and two splits) are loaded at once rather than one row after
+// another.
 template <int D>
 __device__ __noinline__ void split_handoff(const Params& p, int bh, int r0, int n_run, int lane) {
   __threadfence();  // this warp's partials are visible device-wide before it is counted
@@ -222,40 +252,77 @@ __device__ __noinline__ void split_handoff(const Params& p, int bh, int r0, int 
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
   __threadfence();  // the other splits' partials, counted before this warp, are read after their fences
   constexpr int CPL = D / 32;
+  constexpr int RB = 8;  // rows per block of the output pass
   const size_t rows = static_cast<size_t>(p.BH) * p.T;
-  for (int t = r0; t < min(r0 + 32, p.T); ++t) {
-    const size_t r = static_cast<size_t>(bh) * p.T + t;
-    float M = -INFINITY;
-    for (int s = 0; s < n_run; ++s) M = fmaxf(M, __ldcg(p.lsepart + s * rows + r));
-    float acc[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-    float wsum = 0.f;
+  const size_t g0 = static_cast<size_t>(bh) * p.T + r0;  // first row of the group
+  const int nrows = min(32, p.T - r0);
+  const bool live = lane < nrows;
+  const float* lse_l = p.lsepart + g0 + lane;  // this lane's row in split 0's LSE
+  // M and the weight sum in one pass (the sum rescaled whenever the maximum grows), loads four
+  // splits at a time
+  float M = -INFINITY, wsum = 0.f;
+  if (live) {
+#pragma unroll 4
     for (int s = 0; s < n_run; ++s) {
-      const float w = expf(__ldcg(p.lsepart + s * rows + r) - M);
-      wsum += w;
-      const float* src = p.opart + (s * rows + r) * D + lane * CPL;
-      if (CPL == 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2 % CPL] += w * v.z;
-        acc[3 % CPL] += w * v.w;
+      const float x = __ldcg(lse_l + s * rows);
+      if (x > M) {
+        wsum = wsum * expf(M - x) + 1.f;  // M = -inf at first: 0 * 0 + 1
+        M = x;
       } else {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
+        wsum += expf(x - M);
       }
     }
-    const float inv = 1.f / wsum;
-    __nv_bfloat16* dst = p.o + r * D + lane * CPL;
-    if (CPL == 4) {
-      *reinterpret_cast<uint2*>(dst) =
-          make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2 % CPL] * inv, acc[3 % CPL] * inv));
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    p.lse[g0 + lane] = M + logf(wsum);
+  }
+  const float inv = live ? 1.f / wsum : 0.f;
+  for (int t0 = 0; t0 < nrows; t0 += RB) {
+    float acc[RB][CPL];
+#pragma unroll
+    for (int t = 0; t < RB; ++t)
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[t][c] = 0.f;
+#pragma unroll 2
+    for (int s = 0; s < n_run; ++s) {
+      const float wl = live ? expf(__ldcg(lse_l + s * rows) - M) * inv : 0.f;  // row r0 + lane's weight
+      const float* src = p.opart + (s * rows + g0 + t0) * D + lane * CPL;
+      float v[RB][CPL];
+#pragma unroll
+      for (int t = 0; t < RB; ++t) {
+        if (t0 + t < nrows) {
+          if (CPL == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + t * D));
+            v[t][0] = x.x;
+            v[t][1] = x.y;
+            v[t][2 % CPL] = x.z;
+            v[t][3 % CPL] = x.w;
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(src + t * D));
+            v[t][0] = x.x;
+            v[t][1] = x.y;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) v[t][c] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < RB; ++t) {
+        const float w = __shfl_sync(0xffffffffu, wl, t0 + t);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[t][c] += w * v[t][c];
+      }
     }
-    if (lane == 0) p.lse[r] = M + logf(wsum);
+#pragma unroll
+    for (int t = 0; t < RB; ++t) {
+      if (t0 + t >= nrows) break;
+      __nv_bfloat16* dst = p.o + (g0 + t0 + t) * D + lane * CPL;
+      if (CPL == 4) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[t][0], acc[t][1]),
+                                                    pack_bf16x2(acc[t][2 % CPL], acc[t][3 % CPL]));
+      } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[t][0], acc[t][1]);
+      }
+    }
   }
 }
 
@@ -283,6 +350,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t bar_o_empty = barx + 48;  // [2]
   const uint32_t bar_s_free = barx + 64;   // [2] (SEP_P: one phase per S_i read, 4 arrivals)
   const uint32_t bar_done = barx + 80;
+  const uint32_t bar_unit_full = barx + 88;    // [4] claimed work items (see claimed_item)
+  const uint32_t bar_unit_empty = barx + 120;  // [4]
+  const uint32_t unit_slots = sbase + L::MISC_OFF + 16;  // [4] s32
+  // items are claimed at run time, and heads grouped, only in the unsplit bf16 d = 128 kernel
+  // (the host sets p.sched and p.head_group for no other); every other instantiation keeps the
+  // static order and compiles none of this code
+  constexpr bool CLAIM = D == 128 && !F8 && !PARTIAL;
+  const bool claimed = CLAIM && p.sched != nullptr;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
   // SEP_P: S reads of query tile i whose softmax step has ended, 4 per S (one per softmax warp of
@@ -310,6 +385,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(bar_s_free + 8 * i, 4);
     }
     mbar_init(bar_done, L::MMA_WARPS);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(bar_unit_full + 8 * s, 1);
+      mbar_init(bar_unit_empty + 8 * s, 8 + L::MMA_WARPS);  // every softmax and MMA warp reads each item
+    }
     *abort_flag = 0;
     reinterpret_cast<uint32_t*>(smem + L::MISC_OFF + 8)[0] = 0;
     reinterpret_cast<uint32_t*>(smem + L::MISC_OFF + 8)[1] = 0;
@@ -342,7 +421,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tma_prefetch_desc(&tmV);
     const int w = unit_of(0, blockIdx.x, G);
     if (w < p.num_units) {
-      const Unit u = decode_unit<PARTIAL>(p, w);
+      const Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
       const int nmax = max(u.n0, u.n1);
       if (nmax > 0) {
         for (int i = 0; i < 2; ++i)
@@ -374,10 +453,30 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       bool ok = true;
       int nu = 0;  // units this CTA has started
       int bal = 0;
-      for (int k = 0; ok && k * G < p.num_units; ++k) {
-        const int w = unit_of(k, blockIdx.x, G);
-        if (w >= p.num_units) continue;
-        Unit u = decode_unit<PARTIAL>(p, w);
+      int w_next = -1;  // claimed items: the item after the current one, claimed one unit ahead
+      for (int k = 0; ok; ++k) {
+        int w;
+        if (claimed) {
+          w = k == 0 ? int(blockIdx.x) : w_next;
+          if (k > 0) {  // hand item k to the other warps (see claimed_item)
+            const int j = k - 1, s = j & 3;
+            if (!(ok = wait_all(W, bar_unit_empty + 8 * s, ((j >> 2) & 1) ^ 1))) break;
+            if (lane == 0) {
+              asm volatile("st.shared.s32 [%0], %1;" ::"r"(unit_slots + 4 * s), "r"(w) : "memory");
+              mbar_arrive(bar_unit_full + 8 * s);
+            }
+            __syncwarp();
+          }
+          if (w >= p.num_units) break;
+          int c = 0;
+          if (lane == 0) c = atomicAdd(p.sched, 1);
+          w_next = G + __shfl_sync(0xffffffffu, c, 0);
+        } else {
+          if (k * G >= p.num_units) break;
+          w = unit_of(k, blockIdx.x, G);
+          if (w >= p.num_units) continue;
+        }
+        Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
         if (L::SEP_P) balance_slots(u, bal);
         const int nmax = max(u.n0, u.n1);
         if (nmax == 0) continue;  // an empty key split: no role touches it
@@ -401,10 +500,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         q_parity = (q_parity & ~(1u << qb)) | (qpar << qb);
         ++nu;
         if (L::QBUF == 1) {  // warm L2 with the next unit's query tiles
-          int k2 = k + 1, w2 = unit_of(k2, blockIdx.x, G);
-          if (w2 >= p.num_units && (k2 + 1) * G < p.num_units) w2 = unit_of(++k2, blockIdx.x, G);
-          if (w2 < p.num_units) {
-            const Unit u2 = decode_unit<PARTIAL>(p, w2);
+          int w2 = w_next;
+          if (!claimed) {
+            int k2 = k + 1;
+            w2 = unit_of(k2, blockIdx.x, G);
+            if (w2 >= p.num_units && (k2 + 1) * G < p.num_units) w2 = unit_of(++k2, blockIdx.x, G);
+          }
+          if (w2 >= 0 && w2 < p.num_units) {
+            const Unit u2 = decode_unit<PARTIAL, CLAIM>(p, w2);
             for (int i = 0; i < 2; ++i)
               if ((i ? u2.n1 : u2.n0) > 0)
                 for (int b = 0; b < L::BOXES; ++b)
@@ -510,10 +613,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       bool ok = true;
       int nu = 0;
       int bal = 0;
-      for (int k = 0; ok && k * G < p.num_units; ++k) {
-        const int w = unit_of(k, blockIdx.x, G);
+      for (int k = 0; ok; ++k) {
+        const int w = claimed ? claimed_item(p, W, unit_slots, bar_unit_full, bar_unit_empty, k, ok)
+                              : (k * G < p.num_units ? unit_of(k, blockIdx.x, G) : -1);
+        if (w < 0) break;
         if (w >= p.num_units) continue;
-        Unit u = decode_unit<PARTIAL>(p, w);
+        Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
         balance_slots(u, bal);
         const int n = i ? u.n1 : u.n0, nmax = max(u.n0, u.n1);
         if (nmax == 0) continue;
@@ -658,10 +763,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       uint32_t pf0 = 0, pf1 = 0, oe0 = 0, oe1 = 0;
       bool ok = true;
       int nu = 0;
-      for (int k = 0; ok && k * G < p.num_units; ++k) {
-        const int w = unit_of(k, blockIdx.x, G);
+      for (int k = 0; ok; ++k) {
+        const int w = claimed ? claimed_item(p, W, unit_slots, bar_unit_full, bar_unit_empty, k, ok)
+                              : (k * G < p.num_units ? unit_of(k, blockIdx.x, G) : -1);
+        if (w < 0) break;
         if (w >= p.num_units) continue;
-        const Unit u = decode_unit<PARTIAL>(p, w);
+        const Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
         const int n0 = u.n0, n1 = u.n1, nmax = max(n0, n1);
         if (nmax == 0) continue;
         const int last_i = n1 > 0 ? 1 : 0;
@@ -791,10 +898,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     uint32_t sf_phase = 0, of_phase = 0;
     bool ok = true;
     int bal = 0;
-    for (int k = 0; ok && k * G < p.num_units; ++k) {
-      const int w = unit_of(k, blockIdx.x, G);
+    for (int k = 0; ok; ++k) {
+      const int w = claimed ? claimed_item(p, W, unit_slots, bar_unit_full, bar_unit_empty, k, ok)
+                            : (k * G < p.num_units ? unit_of(k, blockIdx.x, G) : -1);
+      if (w < 0) break;
       if (w >= p.num_units) continue;
-      Unit u = decode_unit<PARTIAL>(p, w);
+      Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
       if (L::SEP_P) balance_slots(u, bal);
       const int n = i ? u.n1 : u.n0;
       if (n == 0) continue;
@@ -1016,6 +1125,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  // claimed items: every warp of this CTA is past its last claim; the launch's last CTA to get
+  // here zeroes the counter pair for the next launch that takes this slot (a dependent launch
+  // reads it only after griddepcontrol.wait, i.e. after this grid has completed)
+  if (claimed && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == int(gridDim.x) - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
+    }
+  }
 }
 
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
@@ -1111,40 +1230,70 @@ cudaError_t launch_fa_fwd_e4m3(const CUtensorMap& q, const CUtensorMap& k, const
 
 int fa_fwd_e4m3_smem_bytes() { return Layout<128, true>::SMEM_BYTES; }
 
-// V (rows of 128 e4m3 bytes per key) -> V^T (rows of Tp bytes per channel), keys past T
-// zero: a 64 x 64 byte tile per block through shared memory, 16-byte loads and stores.
+// V (rows of 128 e4m3 bytes per key) -> V^T (rows of Tp bytes per channel), keys past T zero.
+// A block moves 64 keys x 128 channels through shared memory.  In the load phase thread
+// (kg, cg) = (warp, lane) reads keys 8 kg .. 8 kg + 7 at channels 4 cg .. 4 cg + 3, one 4-byte
+// word per key (each warp instruction reads one whole 128-byte row of V), turns the 8 x 4
+// bytes into 4 channels x 8 keys with byte permutes, and stores one 8-byte word per channel;
+// in the store phase thread (c, h) writes channel c's keys 32 h .. 32 h + 31 as two 16-byte
+// words.  In shared memory row c holds channel c's 64 keys as eight 8-byte chunks, chunk k at
+// position k ^ ((c / 4) % 8), so that each phase's accesses spread over the banks.
 __global__ void __launch_bounds__(256) fa_transpose_e4m3_kernel(const uint8_t* __restrict__ v,
                                                                 uint8_t* __restrict__ vt, int T, int Tp) {
-  __shared__ uint8_t tile[64][64 + 16];
-  const int bh = blockIdx.z, c0 = blockIdx.y * 64, t0 = blockIdx.x * 64;
+  __shared__ __align__(16) uint8_t tile[128 * 64];
+  // the attention kernel that reads V^T may start its set-up; its griddepcontrol.wait still
+  // waits for this whole grid
+  pdl_launch_dependents();
+  const int bh = blockIdx.y, t0 = blockIdx.x * 64;
   const uint8_t* src = v + static_cast<size_t>(bh) * T * 128;
   uint8_t* dst = vt + static_cast<size_t>(bh) * 128 * Tp;
-  // 64 keys x 64 channels: each thread loads 16 bytes (one key, 16 channels)
   {
-    const int r = threadIdx.x / 4, cc = (threadIdx.x % 4) * 16;
-    const int t = t0 + r;
-    uint4 x = make_uint4(0, 0, 0, 0);
-    if (t < T) x = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(t) * 128 + c0 + cc);
-    const uint8_t* b = reinterpret_cast<const uint8_t*>(&x);
+    const int cg = threadIdx.x % 32, kg = threadIdx.x / 32;
+    uint32_t w[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) tile[cc + i][r] = b[i];
+    for (int i = 0; i < 8; ++i) {
+      const int t = t0 + 8 * kg + i;
+      w[i] = t < T ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(t) * 128) + cg) : 0u;
+    }
+    uint32_t ch[4][2];  // [channel 4 cg + j][keys 0-3 | 4-7 of the eight]
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t a01 = __byte_perm(w[4 * h], w[4 * h + 1], 0x5140);  // bytes 0, 1 of both, interleaved
+      const uint32_t a23 = __byte_perm(w[4 * h + 2], w[4 * h + 3], 0x5140);
+      const uint32_t b01 = __byte_perm(w[4 * h], w[4 * h + 1], 0x7362);  // bytes 2, 3 of both, interleaved
+      const uint32_t b23 = __byte_perm(w[4 * h + 2], w[4 * h + 3], 0x7362);
+      ch[0][h] = __byte_perm(a01, a23, 0x5410);
+      ch[1][h] = __byte_perm(a01, a23, 0x7632);
+      ch[2][h] = __byte_perm(b01, b23, 0x5410);
+      ch[3][h] = __byte_perm(b01, b23, 0x7632);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint2*>(tile + (4 * cg + j) * 64 + 8 * (kg ^ (cg % 8))) = make_uint2(ch[j][0], ch[j][1]);
   }
   __syncthreads();
-  // 64 channels x 64 keys: each thread stores 16 bytes (one channel, 16 keys)
   {
-    const int c = threadIdx.x / 4, tt = (threadIdx.x % 4) * 16;
-    if (t0 + tt < Tp) {  // Tp is a multiple of 16, so the whole 16-byte group is inside
-      uint4 x;
-      uint8_t* b = reinterpret_cast<uint8_t*>(&x);
+    const int c = threadIdx.x / 2, h = threadIdx.x % 2;
+    const int sw = (c / 4) % 8;
+    uint32_t o[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) b[i] = tile[c][tt + i];
-      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c0 + c) * Tp + t0 + tt) = x;
+    for (int m = 0; m < 4; ++m) {
+      const uint2 x = *reinterpret_cast<const uint2*>(tile + c * 64 + 8 * ((4 * h + m) ^ sw));
+      o[2 * m] = x.x;
+      o[2 * m + 1] = x.y;
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int tt = t0 + 32 * h + 16 * q;
+      if (tt < Tp)  // Tp is a multiple of 16, so the whole 16-byte word is inside
+        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c) * Tp + tt) =
+            make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
     }
   }
 }
 
 cudaError_t launch_transpose_e4m3(const void* v, void* vt, int BH, int T, int Tp, cudaStream_t stream) {
-  const dim3 grid((Tp + 63) / 64, 2, BH);
+  const dim3 grid((Tp + 63) / 64, BH);
   fa_transpose_e4m3_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt),
                                                       T, Tp);
   return cudaGetLastError();
@@ -1175,12 +1324,21 @@ cudaError_t launch_fa_fwd_partial(int d, const CUtensorMap& q, const CUtensorMap
 // not seen before.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Counter pairs of the launches whose work items are claimed at run time (see claimed_item):
+// one pair every kSchedStride ints (a 128-byte line each), zero at load time, and zeroed again
+// by the last CTA of every launch that used the pair.
+static __device__ __align__(128) int g_sched[kSchedSlots * kSchedStride];
+
 namespace {
 using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-}  // namespace
 
-cudaError_t noalloc_scratch_address(void** out) {
+// Device address of the __device__ variable whose host shadow is `symbol`, in the current CUDA
+// context: looked up with cudaGetSymbolAddress on the first call in each context, then cached
+// by the context's process-unique id (up to 64 contexts, the oldest replaced after that).  One
+// cache per Tag.
+template <int Tag>
+cudaError_t context_symbol_address(const void* symbol, void** out) {
   struct Entry {
     unsigned long long ctx_id;
     void* addr;
@@ -1208,7 +1366,7 @@ cudaError_t noalloc_scratch_address(void** out) {
   if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) {
     // no context current yet: the symbol lookup below makes the device's primary context current
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, symbol);
     if (e != cudaSuccess) return e;
     if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
   }
@@ -1218,13 +1376,25 @@ cudaError_t noalloc_scratch_address(void** out) {
       return cudaSuccess;
     }
   void* p = nullptr;
-  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // in the current context
+  const cudaError_t e = cudaGetSymbolAddress(&p, symbol);  // in the current context
   if (e != cudaSuccess) return e;
   Entry& slot = used < 64 ? cache[used++] : cache[next++ % 64];
   slot.ctx_id = id;
   slot.addr = p;
   *out = p;
   return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t noalloc_scratch_address(void** out) {
+  return context_symbol_address<0>(static_cast<const void*>(g_noalloc_scratch), out);
+}
+
+cudaError_t sched_counters_address(int** out) {
+  void* p = nullptr;
+  const cudaError_t e = context_symbol_address<1>(static_cast<const void*>(g_sched), &p);
+  *out = static_cast<int*>(p);
+  return e;
 }
 
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, cudaStream_t stream) {

@@ -35,6 +35,13 @@ struct Params {
   float* lsepart;             // [num_splits][BH*T] fp32 partial LSE (natural log)
   int* counters;              // [BH][ngroups] splits finished per 32-row group (zero at launch)
   int ngroups;                // ceil(T / 32)
+  // order of the work items (unsplit causal launches): head_group > 0 lists the units band by
+  // band within groups of head_group heads (head_group divides BH), so that the CTAs running
+  // at one time read the K / V of a few heads; sched != nullptr hands the items out in that
+  // order from a device-wide counter pair (sched[0]: items claimed after each CTA's first,
+  // sched[1]: CTAs finished; both zero at launch, and the launch's last CTA zeroes them again)
+  int head_group;
+  int* sched;
 };
 
 // Rows per box of the output tensor map `o` (bf16 (d, T, B*H), 128-byte swizzle): each
@@ -67,6 +74,13 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 // Device address of that scratch in the current CUDA context; looked up on the first
 // call in each context (cudaGetSymbolAddress), then cached by the context's unique id.
 cudaError_t noalloc_scratch_address(void** out);
+
+// Counter pairs for launches whose work items are claimed at run time: kSchedSlots pairs, one
+// every kSchedStride ints; a launch takes the next slot in turn.  Returns the device address of
+// the first pair in the current CUDA context (looked up once per context, like the scratch).
+constexpr int kSchedSlots = 64;
+constexpr int kSchedStride = 32;
+cudaError_t sched_counters_address(int** out);
 
 // ---------------------------------------------------------------- backward pass (fa_bwd.cu)
 

@@ -113,10 +113,14 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
  *   q .. scale, stream : as for fa_fwd.
  *   num_splits : 1 .. FA_MAX_SPLITS; the keys (ceil(T / 128) tiles of 128) are
  *                cut into ceil(tiles / ceil(tiles / num_splits)) ranges of
- *                equal tile count.  0 chooses the count: enough splits that
- *                the longest unit's share of the keys fits in the average work
- *                per SM of the current device, at most 16 (1 when the work
- *                units alone balance the SMs).
+ *                equal tile count.  0 chooses the count: the library replays
+ *                the persistent grid's static schedule on the host for 1 .. 16
+ *                splits (costs counted in 128-key steps, with a fixed cost per
+ *                unit and per merge) and takes the count with the shortest
+ *                busiest SM, if it beats one split by at least 10 %.  When the
+ *                count comes to one range, the call is fa_fwd (no partials,
+ *                no merge, the workspace untouched; the result is bit-identical
+ *                to fa_fwd's).
  *   workspace  : caller-owned device memory of at least
  *                fa_fwd_splitkv_workspace_bytes(B, H, T, d, num_splits) bytes,
  *                16-byte aligned, not overlapping any tensor argument.  Its
@@ -264,6 +268,16 @@ fa_status fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, vo
  * device (the larger of the causal and non-causal choices).
  */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int T, int d, int num_splits);
+
+/*
+ * Number of key ranges fa_fwd_splitkv (and fa_fwd_splitkv_noalloc) would use
+ * for these arguments on the current device: num_splits = 0 resolved as
+ * described at fa_fwd_splitkv, then ceil(tiles / ceil(tiles / num_splits))
+ * with tiles = ceil(T / 128).  1 means the call runs fa_fwd.  Returns -1 for
+ * invalid sizes or num_splits, or when no CUDA device is current (num_splits
+ * = 0 only).  No device work.
+ */
+int fa_fwd_splitkv_count(int B, int H, int T, int d, int causal, int num_splits);
 
 /* A static, human-readable name for a status code. */
 const char* fa_status_string(fa_status s);

@@ -107,6 +107,18 @@ def test_splitkv_workspace_size(lib):
         assert fa.fa_fwd_splitkv_workspace_bytes(*bad) == 0
 
 
+def test_splitkv_count(lib):
+    # explicit counts: ceil(tiles / ceil(tiles / num_splits)) key ranges of equal tile count
+    assert fa.fa_fwd_splitkv_count(1, 4, 8192, 128, True, 1) == 1
+    assert fa.fa_fwd_splitkv_count(1, 4, 8192, 128, True, 3) == 3      # 64 tiles: 3 ranges of 22
+    assert fa.fa_fwd_splitkv_count(1, 4, 1000, 64, False, 5) == 4      # 8 tiles: ranges of 2
+    assert fa.fa_fwd_splitkv_count(1, 4, 100, 64, False, 4) == 1       # one tile
+    assert fa.fa_fwd_splitkv_count(2, 3, 1000, 128, True, 8) == 8
+    for bad in ((0, 1, 1, 64, 0, 1), (1, 1, 1, 96, 0, 1), (1, 1, 1, 64, 2, 1), (1, 1, 1, 64, 0, -1),
+                (1, 1, 1, 64, 0, fa.FA_MAX_SPLITS + 1)):
+        assert lib.fa_fwd_splitkv_count(*bad) == -1
+
+
 @pytest.mark.parametrize("ns,ws,code", [(-1, A + 0x5000, 9), (fa.FA_MAX_SPLITS + 1, A + 0x5000, 9)])
 def test_splitkv_host_validation(lib, ns, ws, code):
     rc = lib.fa_fwd_splitkv(A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 1, 2, 128, 64, 0,

@@ -10,7 +10,7 @@ import pytest
 
 import fa_inputs as fi
 import oracle
-from parity import compare, default_scale, rounding_bound, run_gpu, sampled_rows, to_device
+from parity import bf16_to_f64, compare, default_scale, rounding_bound, run_gpu, sampled_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -174,3 +174,38 @@ def test_ex2_rate_probe():
     # one GB300: 152 SMs at 1-2.1 GHz issuing at most one ex2 per lane per cycle
     assert 1e12 < rate < 152 * 128 * 2.2e9
     assert fa.fa_device_status() == 0
+
+
+def test_claimed_order_long_causal():
+    """Causal d = 128 launches whose K and V exceed 96 MB list their units by groups of heads and
+    claim them at run time (B1 H6 T16384: 101 MB, two heads per group).  The result must be the
+    statically ordered launch's bit for bit (a one-range split launch keeps the static order), over
+    more launches than there are counter pairs (so every pair is reused after its reset), and must
+    match the oracle on sampled rows."""
+    import torch
+
+    import exact_io_aware_07_gb300 as fa
+
+    B, H, T, d = 1, 6, 16384, 128
+    qkv = fi.make_qkv(B, H, T, d, seed=12)
+    q, k, v = (to_device(None, b) for b in (qkv.q_bits, qkv.k_bits, qkv.v_bits))
+    scale = default_scale(d)
+    ws = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(B, H, T, d, 1), dtype=torch.uint8, device="cuda")
+    o_st = torch.empty_like(q)
+    l_st = torch.empty(B, H, T, device="cuda")
+    fa.fa_fwd_splitkv(q, k, v, o_st, l_st, True, scale, 1, ws)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, T), float("nan"), device="cuda")
+    for it in range(70):
+        fa.fa_fwd(q, k, v, o, lse, True, scale)
+        if it in (0, 69):
+            torch.cuda.synchronize()
+            assert fa.fa_device_status() == 0
+            assert torch.equal(o.view(torch.int16), o_st.view(torch.int16)) and torch.equal(lse, l_st), f"call {it}"
+    rows = sampled_rows(T, seed=8, first=128, last=128, random=256)
+    o_s = bf16_to_f64(o[:, :, rows])
+    l_s = lse[:, :, rows].cpu().numpy().astype(np.float64)
+    q64, k64, v64 = qkv.f64("q"), qkv.f64("k"), qkv.f64("v")
+    O_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, True, scale, rows=rows)
+    compare(o_s, l_s, O_ref, lse_ref, label=f"claimed order B{B} H{H} T{T} d{d} causal ({rows.size} rows per head)",
+            bound=rounding_bound(q64, k64, v64, True, scale, rows))

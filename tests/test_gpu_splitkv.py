@@ -134,3 +134,28 @@ def test_splitkv_rejects_bad_workspace():
     assert call(ws.data_ptr(), need) == 0
     torch.cuda.synchronize()
     assert fa.fa_device_status() == 0
+
+
+@pytest.mark.parametrize("T,num_splits,causal", [(1000, 1, 1), (100, 4, 0), (200, 1, 0)])
+def test_one_key_range_is_the_plain_kernel(T, num_splits, causal):
+    """A count that comes to one key range (num_splits 1, or T within one tile) runs fa_fwd itself:
+    the same bits, and the workspace is left as it was."""
+    import torch
+
+    import exact_io_aware_07_gb300 as fa
+
+    qkv = fi.make_qkv(2, 3, T, 128, seed=26)
+    q, k, v = (to_device(None, b) for b in (qkv.q_bits, qkv.k_bits, qkv.v_bits))
+    scale = default_scale(128)
+    ws = torch.full((fa.fa_fwd_splitkv_workspace_bytes(2, 3, T, 128, num_splits),), 0x5A, dtype=torch.uint8,
+                    device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    fa.fa_fwd_splitkv(q, k, v, o, lse, causal, scale, num_splits, ws)
+    o_ref = torch.empty_like(q)
+    lse_ref = torch.empty_like(lse)
+    fa.fa_fwd(q, k, v, o_ref, lse_ref, causal, scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16)) and torch.equal(lse, lse_ref)
+    assert bool((ws == 0x5A).all())
