@@ -330,19 +330,23 @@ int auto_splits(int B, int H, int T, int causal, int num_sms) {
 // Order of the work items of an unsplit launch.  Causal bf16 d = 128 launches whose K and V
 // (one K/V head per query head) exceed 96 MB over all heads, so that L2 cannot hold what the
 // CTAs running at one time stream when every head is in flight: the units are listed band by
-// band within groups of heads whose K and V fit in 48 MB, and claimed at run time from one of
-// the library's counter pairs (taken in turn), so that the CTAs running at one time work on
-// one or two groups' heads while claiming in list order keeps the longest units first and the
-// SMs evenly loaded.  Every other launch keeps the static band-by-band (causal) or head-by-head
-// order.  If the counters cannot be found the static order is kept.
+// band within groups of heads whose K and V fit in 48 MB, except the lightest eighth of the
+// bands, which come last band by band over all heads; the CTAs claim the units at run time,
+// in list order, from one of the library's counter pairs (taken in turn).  The CTAs running
+// at one time then work on one or two groups' heads, and claiming a longest-first list that
+// ends in short units keeps the SMs evenly loaded.  Every other launch keeps the static
+// band-by-band (causal) or head-by-head order.  If the counters cannot be found the static
+// order is kept.
 void choose_order(fa::Params& p, int d, int group) {
+  constexpr double kGroupBytes = 48e6;
   p.head_group = 0;
   p.sched = nullptr;
   if (!p.causal || d != 128 || group != 1) return;
   const double head_kv = static_cast<double>(p.T) * d * 2 * 2;  // bytes of K and V of one head
   if (head_kv * p.BH <= 96e6) return;
-  int g = std::max(1, std::min(p.BH, static_cast<int>(48e6 / head_kv)));
+  int g = std::max(1, std::min(p.BH, static_cast<int>(kGroupBytes / head_kv)));
   while (p.BH % g != 0) --g;
+  p.tail_bands = std::max(1, p.nqb / 8);
   int* base = nullptr;
   if (fa::sched_counters_address(&base) != cudaSuccess || !base) {
     cudaGetLastError();

@@ -162,11 +162,19 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
     const int rem = w - band * per_band;
     s = rem / p.BH;
     u.bh = rem - s * p.BH;
-  } else if (GROUPED && p.head_group > 0) {  // causal: band by band within each group of head_group heads
-    const int per_group = p.head_group * p.nqb;
-    const int g = w / per_group, r = w - g * per_group;
-    band = r / p.head_group;
-    u.bh = g * p.head_group + (r - band * p.head_group);
+  } else if (GROUPED && p.head_group > 0) {  // causal: band by band within each group of head_group heads,
+    const int main_bands = p.nqb - p.tail_bands;  // then the lightest bands band by band over all heads
+    const int main_units = p.BH * main_bands;
+    if (w < main_units) {
+      const int per_group = p.head_group * main_bands;
+      const int g = w / per_group, r = w - g * per_group;
+      band = r / p.head_group;
+      u.bh = g * p.head_group + (r - band * p.head_group);
+    } else {
+      const int t = w - main_units, b2 = t / p.BH;
+      band = main_bands + b2;
+      u.bh = t - b2 * p.BH;
+    }
   } else {  // one division: w = first * unit_div + second
     const int first = w / p.unit_div, second = w - first * p.unit_div;
     band = p.causal ? first : second;
@@ -488,25 +496,26 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t qpar = (nu / L::QBUF) & 1;
         if (!(ok = wait_all(W, bar_q_empty + 8 * qb, qpar ^ 1))) break;
         mbar_arrive_expect_tx_elect(bar_q_full + 8 * qb, ((u.n0 > 0) + (u.n1 > 0)) * L::TILE_BYTES);
+        // query tiles are read once (and output tiles written once): in L2 they go before K and V
+        const uint64_t pol_once = l2_policy_evict_first();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if ((i ? u.n1 : u.n0) == 0) continue;
 #pragma unroll
           for (int b = 0; b < L::BOXES; ++b)
-            tma_load_3d_elect(q_smem + (2 * qb + i) * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64,
-                        u.qb * 2 * BM + (i ^ u.sw) * BM, u.bh, bar_q_full + 8 * qb);
+            tma_load_3d_elect_hint(q_smem + (2 * qb + i) * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64,
+                                   u.qb * 2 * BM + (i ^ u.sw) * BM, u.bh, bar_q_full + 8 * qb, pol_once);
         }
         q_issued |= 1u << qb;
         q_parity = (q_parity & ~(1u << qb)) | (qpar << qb);
         ++nu;
-        if (L::QBUF == 1) {  // warm L2 with the next unit's query tiles
-          int w2 = w_next;
-          if (!claimed) {
-            int k2 = k + 1;
-            w2 = unit_of(k2, blockIdx.x, G);
-            if (w2 >= p.num_units && (k2 + 1) * G < p.num_units) w2 = unit_of(++k2, blockIdx.x, G);
-          }
-          if (w2 >= 0 && w2 < p.num_units) {
+        // warm L2 with the next unit's query tiles (not with claimed items: those launches'
+        // K / V stream fills L2, and a prefetched Q tile was often evicted before its load,
+        // so that it came from DRAM twice)
+        if (L::QBUF == 1 && !claimed) {
+          int k2 = k + 1, w2 = unit_of(k2, blockIdx.x, G);
+          if (w2 >= p.num_units && (k2 + 1) * G < p.num_units) w2 = unit_of(++k2, blockIdx.x, G);
+          if (w2 < p.num_units) {
             const Unit u2 = decode_unit<PARTIAL, CLAIM>(p, w2);
             for (int i = 0; i < 2; ++i)
               if ((i ? u2.n1 : u2.n0) > 0)
@@ -1103,7 +1112,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           __syncwarp();
           if (y0 < p.T) {
             if (lane == 0) {
-              tma_store_3d(&tmO, buf, h * 64, y0, u.bh);
+              tma_store_3d_hint(&tmO, buf, h * 64, y0, u.bh, l2_policy_evict_first());
               bulk_commit_group();
             }
             stg_busy = true;

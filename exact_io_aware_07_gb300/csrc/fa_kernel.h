@@ -37,10 +37,13 @@ struct Params {
   int ngroups;                // ceil(T / 32)
   // order of the work items (unsplit causal launches): head_group > 0 lists the units band by
   // band within groups of head_group heads (head_group divides BH), so that the CTAs running
-  // at one time read the K / V of a few heads; sched != nullptr hands the items out in that
-  // order from a device-wide counter pair (sched[0]: items claimed after each CTA's first,
-  // sched[1]: CTAs finished; both zero at launch, and the launch's last CTA zeroes them again)
+  // at one time read the K / V of a few heads, except the lightest tail_bands bands, which
+  // follow band by band over all heads (short units last, whatever their head); sched !=
+  // nullptr hands the items out in that order from a device-wide counter pair (sched[0]: items
+  // claimed after each CTA's first, sched[1]: CTAs finished; both zero at launch, and the
+  // launch's last CTA zeroes them again)
   int head_group;
+  int tail_bands;             // head_group > 0: the lightest tail_bands bands of every head come last, band by band
   int* sched;
 };
 

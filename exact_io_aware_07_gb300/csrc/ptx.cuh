@@ -386,6 +386,28 @@ __device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void* src, u
       "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
 }
+// L2 policy for data touched once (the query tiles, the output): its lines are the first to
+// go when L2 needs room, so that the tiles that are read again (K and V) stay.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// tma_load_3d_elect with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_elect_hint(uint32_t dst, const void* tmap, int x, int y, int z,
+                                                       uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;\n\t}"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol) : "memory");
+}
+// tma_store_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_store_3d_hint(const void* tmap, uint32_t src, int x, int y, int z, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;"
+      :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y), "r"(z), "l"(pol) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_l2_3d_elect(const void* tmap, int x, int y, int z) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
