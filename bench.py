@@ -303,8 +303,9 @@ def run_ours(args, world, rank, local, pg):
     roofline = {
         "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
         "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
-        "traffic_source": (f"ncu capture of one launch of this forward-kernel build (dram__bytes_read.sum + "
-                           f"dram__bytes_write.sum), profiles/{traffic_file}") if traffic else
+        "traffic_source": (f"recorded: a separate ncu capture of one launch of this forward-kernel build, reads "
+                           f"and writes (dram__bytes_read.sum + dram__bytes_write.sum), profiles/{traffic_file}")
+                          if traffic else
                           "no ncu capture of this forward-kernel build on record",
         "peak_source": f"{peak_src} bf16 burst", "kernel": "fa_fwd_kernel",
         "floor_bytes": floor_bytes(B, H, T, d),

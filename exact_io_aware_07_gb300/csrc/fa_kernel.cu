@@ -334,7 +334,10 @@ __device__ __noinline__ void split_handoff(const Params& p, int bh, int r0, int 
   }
 }
 
-template <int D, bool PARTIAL, bool F8 = false>
+// CLAIM: the work items are claimed at run time in head-group order (p.sched, p.head_group set;
+// unsplit bf16 d = 128 only); every other launch takes the static order, in an instantiation
+// that compiles none of the claiming code.
+template <int D, bool PARTIAL, bool F8 = false, bool CLAIM = false>
 __global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Params p) {
@@ -361,11 +364,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t bar_unit_full = barx + 88;    // [4] claimed work items (see claimed_item)
   const uint32_t bar_unit_empty = barx + 120;  // [4]
   const uint32_t unit_slots = sbase + L::MISC_OFF + 16;  // [4] s32
-  // items are claimed at run time, and heads grouped, only in the unsplit bf16 d = 128 kernel
-  // (the host sets p.sched and p.head_group for no other); every other instantiation keeps the
-  // static order and compiles none of this code
-  constexpr bool CLAIM = D == 128 && !F8 && !PARTIAL;
-  const bool claimed = CLAIM && p.sched != nullptr;
+  static_assert(!CLAIM || (D == 128 && !F8 && !PARTIAL), "claimed items: unsplit bf16 d = 128 only");
+  constexpr bool claimed = CLAIM;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
   // SEP_P: S reads of query tile i whose softmax step has ended, 4 per S (one per softmax warp of
@@ -461,11 +461,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       bool ok = true;
       int nu = 0;  // units this CTA has started
       int bal = 0;
-      int w_next = -1;  // claimed items: the item after the current one, claimed one unit ahead
       for (int k = 0; ok; ++k) {
         int w;
         if (claimed) {
-          w = k == 0 ? int(blockIdx.x) : w_next;
+          if (k == 0) {
+            w = int(blockIdx.x);
+          } else {  // claimed when this warp is ready to load it (claiming a unit ahead was 2 % slower)
+            int c = 0;
+            if (lane == 0) c = atomicAdd(p.sched, 1);
+            w = G + __shfl_sync(0xffffffffu, c, 0);
+          }
           if (k > 0) {  // hand item k to the other warps (see claimed_item)
             const int j = k - 1, s = j & 3;
             if (!(ok = wait_all(W, bar_unit_empty + 8 * s, ((j >> 2) & 1) ^ 1))) break;
@@ -476,9 +481,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             __syncwarp();
           }
           if (w >= p.num_units) break;
-          int c = 0;
-          if (lane == 0) c = atomicAdd(p.sched, 1);
-          w_next = G + __shfl_sync(0xffffffffu, c, 0);
         } else {
           if (k * G >= p.num_units) break;
           w = unit_of(k, blockIdx.x, G);
@@ -496,22 +498,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t qpar = (nu / L::QBUF) & 1;
         if (!(ok = wait_all(W, bar_q_empty + 8 * qb, qpar ^ 1))) break;
         mbar_arrive_expect_tx_elect(bar_q_full + 8 * qb, ((u.n0 > 0) + (u.n1 > 0)) * L::TILE_BYTES);
-        // query tiles are read once (and output tiles written once): in L2 they go before K and V
-        const uint64_t pol_once = l2_policy_evict_first();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if ((i ? u.n1 : u.n0) == 0) continue;
 #pragma unroll
-          for (int b = 0; b < L::BOXES; ++b)
-            tma_load_3d_elect_hint(q_smem + (2 * qb + i) * L::TILE_BYTES + b * BOX_BYTES, &tmQ, b * 64,
-                                   u.qb * 2 * BM + (i ^ u.sw) * BM, u.bh, bar_q_full + 8 * qb, pol_once);
+          for (int b = 0; b < L::BOXES; ++b) {
+            const uint32_t dst = q_smem + (2 * qb + i) * L::TILE_BYTES + b * BOX_BYTES;
+            const int y = u.qb * 2 * BM + (i ^ u.sw) * BM;
+            if (claimed)  // query tiles are read once (output tiles written once): in L2 they go before K, V
+              tma_load_3d_elect_hint(dst, &tmQ, b * 64, y, u.bh, bar_q_full + 8 * qb, l2_policy_evict_first());
+            else
+              tma_load_3d_elect(dst, &tmQ, b * 64, y, u.bh, bar_q_full + 8 * qb);
+          }
         }
         q_issued |= 1u << qb;
         q_parity = (q_parity & ~(1u << qb)) | (qpar << qb);
         ++nu;
-        // warm L2 with the next unit's query tiles (not with claimed items: those launches'
-        // K / V stream fills L2, and a prefetched Q tile was often evicted before its load,
-        // so that it came from DRAM twice)
+        // warm L2 with the next unit's query tiles (not with claimed items, whose next unit is not
+        // known yet)
         if (L::QBUF == 1 && !claimed) {
           int k2 = k + 1, w2 = unit_of(k2, blockIdx.x, G);
           if (w2 >= p.num_units && (k2 + 1) * G < p.num_units) w2 = unit_of(++k2, blockIdx.x, G);
@@ -1112,7 +1116,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           __syncwarp();
           if (y0 < p.T) {
             if (lane == 0) {
-              tma_store_3d_hint(&tmO, buf, h * 64, y0, u.bh, l2_policy_evict_first());
+              if (claimed)
+                tma_store_3d_hint(&tmO, buf, h * 64, y0, u.bh, l2_policy_evict_first());
+              else
+                tma_store_3d(&tmO, buf, h * 64, y0, u.bh);
               bulk_commit_group();
             }
             stg_busy = true;
@@ -1203,7 +1210,7 @@ cudaError_t measure_ex2_rate(int num_sms, double* ops_per_second, cudaStream_t s
 
 // ---------------------------------------------------------------- host side
 
-template <int D, bool PARTIAL, bool F8 = false>
+template <int D, bool PARTIAL, bool F8 = false, bool CLAIM = false>
 static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                           const Params& p, int grid, cudaStream_t stream) {
   using L = Layout<D, F8>;
@@ -1212,7 +1219,7 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_fwd_kernel<D, PARTIAL, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_fwd_kernel<D, PARTIAL, F8, CLAIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -1227,7 +1234,7 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL, F8>, q, k, v, o, p);
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, PARTIAL, F8, CLAIM>, q, k, v, o, p);
 }
 
 static_assert(Layout<128, true>::SMEM_BYTES <= MAX_SMEM_PER_CTA, "e4m3 layout exceeds the per-CTA limit");
@@ -1311,6 +1318,7 @@ cudaError_t launch_transpose_e4m3(const void* v, void* vt, int BH, int T, int Tp
 cudaError_t launch_fa_fwd(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const Params& p, int grid, cudaStream_t stream) {
   if (d == 64) return launch<64, false>(q, k, v, o, p, grid, stream);
+  if (p.sched) return launch<128, false, false, true>(q, k, v, o, p, grid, stream);
   return launch<128, false>(q, k, v, o, p, grid, stream);
 }
 
