@@ -152,10 +152,16 @@ struct Unit {
 // time then share a few heads' K and V, which stay in L2.  With split keys,
 // split s of a unit covers key tiles [s * split_tiles, (s + 1) * split_tiles)
 // of what each query tile may see.
-template <bool PARTIAL, bool GROUPED>
+template <bool PARTIAL, bool GROUPED, bool HALVES>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
   Unit u;
   int band, s = 0;
+  int half = -1;  // a one-tile item: which query tile of its unit
+  if (HALVES && !PARTIAL && p.halves > 0 && w >= p.num_units - p.halves) {
+    const int t = w - (p.num_units - p.halves);
+    half = t & 1;
+    w = p.num_units - p.halves + (t >> 1);
+  }
   if (PARTIAL) {
     const int per_band = p.BH * p.num_splits;
     band = w / per_band;
@@ -194,6 +200,11 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int w) {
     u.jb = 0;
     u.n0 = e0;
     u.n1 = e1;
+    if (half >= 0) {  // slot 0 takes query tile `half` of the unit, slot 1 nothing
+      u.n0 = half ? e1 : e0;
+      u.n1 = 0;
+      u.sw = half;
+    }
   }
   return u;
 }
@@ -207,7 +218,7 @@ __device__ __forceinline__ void balance_slots(Unit& u, int& bal) {
     const int t = u.n0;
     u.n0 = u.n1;
     u.n1 = t;
-    u.sw = 1;
+    u.sw ^= 1;
   }
   bal += u.n0 - u.n1;
 }
@@ -429,11 +440,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tma_prefetch_desc(&tmV);
     const int w = unit_of(0, blockIdx.x, G);
     if (w < p.num_units) {
-      const Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
+      const Unit u = decode_unit<PARTIAL, CLAIM, F8>(p, w);
       const int nmax = max(u.n0, u.n1);
       if (nmax > 0) {
         for (int i = 0; i < 2; ++i)
-          for (int b = 0; b < L::BOXES; ++b) tma_prefetch_l2_3d(&tmQ, b * 64, u.qb * 2 * BM + i * BM, u.bh);
+          for (int b = 0; b < L::BOXES; ++b) tma_prefetch_l2_3d(&tmQ, b * 64, u.qb * 2 * BM + (i ^ u.sw) * BM, u.bh);
         if (!p.block_table) {
           const int kvh = p.group == 1 ? u.bh : (u.bh / p.H) * (p.H / p.group) + (u.bh % p.H) / p.group;
           for (int j = 0; j < min(nmax, 2); ++j)
@@ -486,7 +497,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           w = unit_of(k, blockIdx.x, G);
           if (w >= p.num_units) continue;
         }
-        Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
+        Unit u = decode_unit<PARTIAL, CLAIM, F8>(p, w);
         if (L::SEP_P) balance_slots(u, bal);
         const int nmax = max(u.n0, u.n1);
         if (nmax == 0) continue;  // an empty key split: no role touches it
@@ -520,11 +531,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           int k2 = k + 1, w2 = unit_of(k2, blockIdx.x, G);
           if (w2 >= p.num_units && (k2 + 1) * G < p.num_units) w2 = unit_of(++k2, blockIdx.x, G);
           if (w2 < p.num_units) {
-            const Unit u2 = decode_unit<PARTIAL, CLAIM>(p, w2);
+            const Unit u2 = decode_unit<PARTIAL, CLAIM, F8>(p, w2);
             for (int i = 0; i < 2; ++i)
               if ((i ? u2.n1 : u2.n0) > 0)
                 for (int b = 0; b < L::BOXES; ++b)
-                  tma_prefetch_l2_3d_elect(&tmQ, b * 64, u2.qb * 2 * BM + i * BM, u2.bh);
+                  tma_prefetch_l2_3d_elect(&tmQ, b * 64, u2.qb * 2 * BM + (i ^ u2.sw) * BM, u2.bh);
           }
         }
         // ring order = the order the MMA warps take tiles in: K_0 V_0 K_1 V_1 ..., or with
@@ -631,7 +642,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                               : (k * G < p.num_units ? unit_of(k, blockIdx.x, G) : -1);
         if (w < 0) break;
         if (w >= p.num_units) continue;
-        Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
+        Unit u = decode_unit<PARTIAL, CLAIM, F8>(p, w);
         balance_slots(u, bal);
         const int n = i ? u.n1 : u.n0, nmax = max(u.n0, u.n1);
         if (nmax == 0) continue;
@@ -781,7 +792,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                               : (k * G < p.num_units ? unit_of(k, blockIdx.x, G) : -1);
         if (w < 0) break;
         if (w >= p.num_units) continue;
-        const Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
+        const Unit u = decode_unit<PARTIAL, CLAIM, F8>(p, w);
         const int n0 = u.n0, n1 = u.n1, nmax = max(n0, n1);
         if (nmax == 0) continue;
         const int last_i = n1 > 0 ? 1 : 0;
@@ -916,7 +927,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                             : (k * G < p.num_units ? unit_of(k, blockIdx.x, G) : -1);
       if (w < 0) break;
       if (w >= p.num_units) continue;
-      Unit u = decode_unit<PARTIAL, CLAIM>(p, w);
+      Unit u = decode_unit<PARTIAL, CLAIM, F8>(p, w);
       if (L::SEP_P) balance_slots(u, bal);
       const int n = i ? u.n1 : u.n0;
       if (n == 0) continue;

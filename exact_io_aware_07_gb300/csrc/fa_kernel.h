@@ -42,6 +42,9 @@ struct Params {
   // nullptr hands the items out in that order from a device-wide counter pair (sched[0]: items
   // claimed after each CTA's first, sched[1]: CTAs finished; both zero at launch, and the
   // launch's last CTA zeroes them again)
+  // non-causal unsplit e4m3 launches: the last `halves` work items are the two query tiles of
+  // the units of a part-empty last round of the grid, one tile per item (0: none)
+  int halves;
   int head_group;
   int tail_bands;             // head_group > 0: the lightest tail_bands bands of every head come last, band by band
   int* sched;

@@ -142,3 +142,36 @@ def test_fp8_rejects_bad_arguments():
     assert call() == 0
     torch.cuda.synchronize()
     assert fa.fa_device_status() == 0
+
+
+def test_fp8_last_round_in_single_tiles():
+    """Non-causal e4m3 launches whose last round of units would leave SMs idle work it in single
+    query tiles (B1 H20 T2048: 160 units on 152 SMs, the last 8 as 16 one-tile items; B1 H4: its 32
+    units as 64 items; B1 H16: 128 whole units).  Each row's arithmetic does not depend on the
+    split, so H20 must equal H16 and H4 on the same heads bit for bit; the oracle checks H4."""
+    import torch
+
+    import exact_io_aware_07_gb300 as fa
+
+    B, H, T, d = 1, 20, 2048, 128
+    x = fi.make_qkv_e4m3(B, H, T, d, seed=73)
+    scale = d ** -0.5
+
+    def run(heads):
+        q, k, v = (torch.from_numpy(np.ascontiguousarray(getattr(x, n + "8")[:, heads])).cuda() for n in "qkv")
+        h = q.shape[1]
+        o = torch.full((B, h, T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((B, h, T), float("nan"), dtype=torch.float32, device="cuda")
+        ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, h, T, d), dtype=torch.uint8, device="cuda")
+        fa.fa_fwd_fp8(q, k, v, o, lse, False, scale, x.descale, ws)
+        return o, lse
+
+    o, lse = run(slice(0, 20))
+    o16, l16 = run(slice(0, 16))
+    o4, l4 = run(slice(16, 20))
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert torch.equal(o.view(torch.int16), torch.cat([o16, o4], 1).view(torch.int16))
+    assert torch.equal(lse, torch.cat([l16, l4], 1))
+    sub = fi.QKV8(B, 4, T, d, x.q8[:, 16:20], x.k8[:, 16:20], x.v8[:, 16:20], x.descale)
+    _check(sub, bf16_to_f64(o4), l4.cpu().numpy().astype(np.float64), False, scale, "fp8 one-tile last round H4 T2048")

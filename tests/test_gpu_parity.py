@@ -209,3 +209,4 @@ def test_claimed_order_long_causal():
     O_ref, lse_ref = oracle.attention_fwd(q64, k64, v64, True, scale, rows=rows)
     compare(o_s, l_s, O_ref, lse_ref, label=f"claimed order B{B} H{H} T{T} d{d} causal ({rows.size} rows per head)",
             bound=rounding_bound(q64, k64, v64, True, scale, rows))
+
