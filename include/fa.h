@@ -22,8 +22,18 @@
  * of shape (B, H, T, d) (d fastest).  LSE is a dense fp32 tensor (B, H, T).
  *
  * Ownership: the caller owns every buffer; all five pointers are device
- * memory of the current CUDA device.  The library allocates no memory and
- * keeps no per-call state.  O and LSE must not overlap Q, K, V or each other.
+ * memory of the current CUDA device.  The library allocates no memory.  O
+ * and LSE must not overlap Q, K, V or each other.
+ *
+ * Shared state: a causal d = 128 fa_fwd whose K and V exceed 96 MB over all
+ * heads hands its work units out at run time from one of 64 counter pairs
+ * that the library holds in device memory (a launch takes the next pair in
+ * turn; its last block zeroes the pair again).  Such launches may run
+ * concurrently on unordered streams as long as fewer than 64 of them are in
+ * flight at once; a CUDA graph that contains one must not be replayed on two
+ * streams at the same time (both replays would share its pair).  The first
+ * such call in a CUDA context looks the pairs' address up (make it before a
+ * stream capture).  Every other call keeps no state between calls.
  *
  * Execution: fa_fwd only validates its arguments and enqueues one kernel on
  * `stream`; it does not synchronise.  O and LSE are complete once the stream
