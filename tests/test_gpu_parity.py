@@ -176,17 +176,19 @@ def test_ex2_rate_probe():
     assert fa.fa_device_status() == 0
 
 
-def test_claimed_order_long_causal():
+@pytest.mark.parametrize("B,H,T,reps", [(1, 6, 16384, 70), (2, 5, 19999, 3)])
+def test_claimed_order_long_causal(B, H, T, reps):
     """Causal d = 128 launches whose K and V exceed 96 MB list their units by groups of heads and
-    claim them at run time (B1 H6 T16384: 101 MB, two heads per group).  The result must be the
-    statically ordered launch's bit for bit (a one-range split launch keeps the static order), over
-    more launches than there are counter pairs (so every pair is reused after its reset), and must
-    match the oracle on sampled rows."""
+    claim them at run time (B1 H6 T16384: 101 MB, two heads per group; B2 H5 T19999: 102 MB, two
+    heads per group, a ragged last band).  The result must be the statically ordered launch's bit
+    for bit (a one-range split launch keeps the static order), over more launches than there are
+    counter pairs in the first case (so every pair is reused after its reset), and must match the
+    oracle on sampled rows."""
     import torch
 
     import exact_io_aware_07_gb300 as fa
 
-    B, H, T, d = 1, 6, 16384, 128
+    d = 128
     qkv = fi.make_qkv(B, H, T, d, seed=12)
     q, k, v = (to_device(None, b) for b in (qkv.q_bits, qkv.k_bits, qkv.v_bits))
     scale = default_scale(d)
@@ -196,9 +198,9 @@ def test_claimed_order_long_causal():
     fa.fa_fwd_splitkv(q, k, v, o_st, l_st, True, scale, 1, ws)
     o = torch.full_like(q, float("nan"))
     lse = torch.full((B, H, T), float("nan"), device="cuda")
-    for it in range(70):
+    for it in range(reps):
         fa.fa_fwd(q, k, v, o, lse, True, scale)
-        if it in (0, 69):
+        if it in (0, reps - 1):
             torch.cuda.synchronize()
             assert fa.fa_device_status() == 0
             assert torch.equal(o.view(torch.int16), o_st.view(torch.int16)) and torch.equal(lse, l_st), f"call {it}"
